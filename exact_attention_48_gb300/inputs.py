@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module holds no attention arithmetic: it only names the workloads and
+draws i.i.d. Gaussian tensors from a seeded generator.  Both the CUDA path
+and the fp64 oracle are fed the very same (bf16-rounded) tensors it returns.
+
+Workloads.  The pages measure on GPT-style training without naming a
+dataset, so dense i.i.d. N(0, 1) tensors of the training shapes stand in for
+it: no padding, no variable lengths, one square mask convention (key j is
+visible to query i iff j <= i when causal).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    backward: bool = True
+    input_mult: float = 1.0   # Q/K/V are N(0,1) * input_mult (dO stays N(0,1))
+    seed: int = 1000
+    note: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops_fwd(self) -> float:
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def flops_bwd(self) -> float:
+        return 2.5 * self.flops_fwd()
+
+
+# The five workload families: a tiny oracle check, a forward-only shape, a
+# causal training shape, a long-context shape and a sequence-length sweep.
+TINY = Workload("tiny_b1h2n128d64", 1, 2, 128, 64, False, True, 1.0, 1000,
+                "oracle check; drawn in fp32, GPU sees the bf16 cast")
+FWD_B8H16N2048D64 = Workload("fwd_b8h16n2048d64", 8, 16, 2048, 64, False, False, 1.0, 1001,
+                             "forward only, non-causal")
+CAUSAL_B4H32N4096D128 = Workload("causal_b4h32n4096d128", 4, 32, 4096, 128, True, True, 1.0, 1002,
+                                 "causal LM training shape")
+LONG_B1H16N16384D128 = Workload("long_b1h16n16384d128x2", 1, 16, 16384, 128, True, True, 2.0, 1003,
+                                "long context, inputs x2 (sharper softmax)")
+
+
+def sweep(N: int, d: int, causal: bool) -> Workload:
+    """B*N fixed at 16384 tokens, H = 16."""
+    B = 16384 // N
+    return Workload(f"sweep_b{B}h16n{N}d{d}{'_causal' if causal else ''}", B, 16, N, d, causal,
+                    True, 1.0, 1004 + N * 10 + d)
+
+
+SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
+HEADLINE = sweep(8192, 128, False)   # B=2, H=16, N=8192, d=128, non-causal
+
+
+def draw(w: Workload, device="cpu", dtype=torch.bfloat16, with_dout: bool = True):
+    """Return (q, k, v, dout) for workload ``w`` as contiguous [B, H, N, d] tensors.
+
+    Values are drawn in fp32 (order q, k, v, dout) from ``torch.Generator``
+    seeded with ``w.seed`` on ``device`` and then cast to ``dtype``.
+    """
+    return draw_shape(w.B, w.H, w.N, w.d, w.seed, w.input_mult, device, dtype, with_dout)
+
+
+def draw_shape(B, H, N, d, seed, input_mult=1.0, device="cpu", dtype=torch.bfloat16,
+               with_dout=True):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shape = (B, H, N, d)
+    out = []
+    for i in range(4 if with_dout else 3):
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if i < 3 and input_mult != 1.0:
+            x = x * input_mult
+        out.append(x.to(dtype).contiguous())
+    if not with_dout:
+        out.append(None)
+    return tuple(out)
