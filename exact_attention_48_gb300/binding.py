@@ -1,0 +1,157 @@
+"""Thin ctypes binding of libfa.so (argument marshalling only).
+
+The functions carry the C-ABI names.  They take torch CUDA tensors, check
+dtype/shape/contiguity, allocate outputs with torch when none are given and
+pass raw device pointers and the current torch stream to the library.  Every
+step of the computation runs in the library's kernels; there is no fallback:
+if ``libfa.so`` is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .build import LIB
+
+_lock = threading.Lock()
+_lib = None
+
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK",
+    1: "FA_ERR_INVALID_ARGUMENT",
+    2: "FA_ERR_UNSUPPORTED",
+    3: "FA_ERR_WORKSPACE",
+    4: "FA_ERR_CUDA",
+    5: "FA_ERR_DEVICE_TIMEOUT",
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+
+
+def library(path: str | None = None):
+    """Load (once) and return the ctypes handle of libfa.so."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"libfa.so not found at {p}; build it with "
+                    "`python -m exact_attention_48_gb300.build` (there is no CPU fallback)")
+            lib = ctypes.CDLL(p)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            lib.fa_fwd.restype = i
+            lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+            lib.fa_bwd_workspace_bytes.restype = sz
+            lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+            lib.fa_bwd.restype = i
+            lib.fa_device_status.argtypes = [vp]
+            lib.fa_device_status.restype = i
+            lib.fa_debug_last_wait_site.argtypes = []
+            lib.fa_debug_last_wait_site.restype = i
+            lib.fa_status_string.argtypes = [i]
+            lib.fa_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return library().fa_status_string(int(code)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_qkv(name, t, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+    """o, lse = softmax(q k^T * scale) v and its natural-log logsumexp.
+
+    q, k, v: contiguous bf16 CUDA tensors [B, H, N, d] (d = 64 or 128).
+    Returns (o [B, H, N, d] bf16, lse [B, H, N] fp32).
+    """
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    _check_qkv("k", k, q.shape)
+    _check_qkv("v", v, q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_qkv("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    rc = library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(library().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dq, dk, dv of a loss through o = attention(q, k, v), given dout and the saved lse.
+
+    ``workspace`` may be a CUDA uint8 tensor of at least
+    ``fa_bwd_workspace_bytes(B, H, N, d)`` bytes (256-byte aligned); if None
+    the library allocates it on the stream.
+    """
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          B, H, N, d, int(bool(causal)), float(scale), ws_ptr, ws_bytes,
+                          _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(library().fa_device_status(_stream_handle(stream)))

@@ -1,0 +1,130 @@
+/*
+ * fa.h -- C ABI of libfa.so, exact scaled-dot-product attention on one GB300.
+ *
+ * The method.  Attention O = softmax(Q K^T * scale) V is computed block by
+ * block in on-chip memory (lexicon page "FlashAttention" (urworte.de),
+ * section "Methodische Grundlagen": "Blockweise Verarbeitung"), with the
+ * score, normalisation and weighting steps fused into one pass
+ * ("Verschmelzung der Schritte") and the row normalisation kept as a running
+ * statistic that corrects earlier partial results when a larger score shows
+ * up ("Fortlaufende Normierung").  The backward pass recomputes the scores
+ * instead of storing them ("Neuberechnung statt Speicherung").  The result
+ * equals the conventional computation up to rounding ("Exaktheit").  The
+ * N x N score matrix never reaches device memory, so memory grows linearly
+ * in N (page "FlashAttention-2 (DE)" (systems-analysis.info), section
+ * "Hintergrund").
+ *
+ * Conventions shared by every call below.
+ *  - Tensors q, k, v, o, dO, dq, dk, dv are bf16, contiguous [B, H, N, d]
+ *    (d fastest).  lse is fp32, contiguous [B, H, N].  All pointers are
+ *    device pointers owned by the caller, 16-byte aligned, non-null, and
+ *    the library keeps none of them after the call returns.
+ *  - B, H, N >= 1; d is 64 or 128 (FA_ERR_UNSUPPORTED otherwise);
+ *    B*H*N*d < 2^31 elements per tensor.
+ *  - causal is 0 or 1.  With causal = 1, key j is visible to query i iff
+ *    j <= i (square mask, aligned at the top-left).  Fully masked tiles are
+ *    skipped.
+ *  - scale is any finite float (the usual value is 1/sqrt(d)).
+ *  - lse[i] = ln sum_{j visible} exp(scale * q_i . k_j): the natural-log
+ *    logsumexp of the SCALED scores.
+ *  - Outputs must not overlap inputs.
+ *  - Every call is asynchronous on `stream` (0 = the legacy default
+ *    stream) and validates all arguments on the host before any CUDA call;
+ *    an invalid call launches nothing and returns an error code.
+ *  - A kernel whose internal pipeline wait runs past its time limit stops,
+ *    records FA_ERR_DEVICE_TIMEOUT in a per-device status word and returns;
+ *    fa_device_status() reads and clears it.  Kernels never trap.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, non-finite scale, bad flag */
+    FA_ERR_UNSUPPORTED = 2,      /* head dimension other than 64 or 128 */
+    FA_ERR_WORKSPACE = 3,        /* caller workspace smaller than fa_bwd_workspace_bytes() */
+    FA_ERR_CUDA = 4,             /* a CUDA runtime/driver call or launch failed */
+    FA_ERR_DEVICE_TIMEOUT = 5    /* a kernel gave up on a pipeline wait (see fa_device_status) */
+} fa_status_t;
+
+/*
+ * Forward pass: o = softmax(q k^T * scale) v and lse (see conventions).
+ * Page "FlashAttention" (urworte.de), "Methodische Grundlagen": tiling,
+ * fused steps and running normalisation; page "FlashAttention-2 (DE)",
+ * "Technische Architektur", section 2: the work of one head is spread over
+ * the SMs by query block.
+ *   q, k, v : inputs  [B, H, N, d] bf16
+ *   o       : output  [B, H, N, d] bf16
+ *   lse     : output  [B, H, N] fp32
+ * Bitwise reproducible from run to run for the same inputs.
+ */
+FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int N, int d, int causal, float scale,
+                   cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
+ * accumulator [B, H, N, d], plus D = rowsum(dO * O) and the logsumexp in
+ * log2 units, each fp32 [B, H, Np] with N padded up to Np, the next
+ * multiple of 128; each part rounded up to 256 bytes.  Linear in N.
+ * Returns 0 for sizes fa_bwd would reject.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: gradients of a loss L through o = attention(q, k, v), given
+ * dO = dL/do and the lse saved by fa_fwd.  The scores and probabilities are
+ * recomputed from q, k and lse; nothing of size N x N is stored (page
+ * "FlashAttention" (urworte.de), "Methodische Grundlagen", paragraph
+ * "Neuberechnung statt Speicherung").
+ *   q, k, v, o, dO : inputs  [B, H, N, d] bf16 (o as written by fa_fwd)
+ *   lse            : input   [B, H, N] fp32 (as written by fa_fwd)
+ *   dq, dk, dv     : outputs [B, H, N, d] bf16
+ *   workspace      : device scratch of at least fa_bwd_workspace_bytes()
+ *                    bytes, 256-byte aligned, or NULL to let the library
+ *                    take it with cudaMallocAsync/cudaFreeAsync on `stream`.
+ * dq is accumulated with fp32 atomics across key blocks, so it is not
+ * bitwise reproducible run to run (differences stay at fp32 rounding level
+ * before the bf16 cast).  dk and dv are reproducible.
+ */
+FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                   const void *dO, const float *lse, void *dq, void *dk, void *dv,
+                   int B, int H, int N, int d, int causal, float scale,
+                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the status word the kernels of the
+ * current device recorded (FA_OK or FA_ERR_DEVICE_TIMEOUT) and resets it to
+ * FA_OK.  Returns FA_ERR_CUDA if the synchronisation itself fails.
+ */
+FA_API fa_status_t fa_device_status(cudaStream_t stream);
+
+/*
+ * Diagnostic: the wait site (a small positive integer naming the pipeline
+ * barrier) of the first timeout recorded on the current device since the
+ * status word was last cleared, 0 if none, -1 if it cannot be read.  Call it
+ * before fa_device_status(), which clears the record.
+ */
+FA_API int fa_debug_last_wait_site(void);
+
+/* A static, NUL-terminated description of a status code. */
+FA_API const char *fa_status_string(fa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

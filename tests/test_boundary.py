@@ -1,0 +1,114 @@
+"""C-ABI boundary on the CPU: the library builds, loads, exports every symbol
+include/fa.h declares, and rejects invalid arguments on the host before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_48_gb300 import build as fa_build
+from exact_attention_48_gb300.binding import library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+FA_OK, FA_ERR_INVALID_ARGUMENT, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return library()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        # every exported declaration starts with FA_API: "FA_API <type> <name>("
+        names += re.findall(r"^\s*FA_API\s+[^(;]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_device_status", "fa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported by libfa.so"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.fa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.fa_status_string(99).decode() == "unknown status"
+
+
+# A fake, 256-byte-aligned, non-null device address: validation must reject
+# each call below before it touches it (or any CUDA API).
+FAKE = 1 << 40
+
+
+def _fwd(lib, *, q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), o=FAKE + (3 << 30), lse=FAKE + (4 << 30),
+         B=1, H=2, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), FA_ERR_INVALID_ARGUMENT),
+    (dict(H=-1), FA_ERR_INVALID_ARGUMENT),
+    (dict(N=0), FA_ERR_INVALID_ARGUMENT),
+    (dict(d=0), FA_ERR_INVALID_ARGUMENT),
+    (dict(d=96), FA_ERR_UNSUPPORTED),
+    (dict(d=256), FA_ERR_UNSUPPORTED),
+    (dict(causal=2), FA_ERR_INVALID_ARGUMENT),
+    (dict(scale=float("nan")), FA_ERR_INVALID_ARGUMENT),
+    (dict(scale=float("inf")), FA_ERR_INVALID_ARGUMENT),
+    (dict(q=0), FA_ERR_INVALID_ARGUMENT),
+    (dict(lse=0), FA_ERR_INVALID_ARGUMENT),
+    (dict(k=FAKE + 8), FA_ERR_INVALID_ARGUMENT),          # misaligned
+    (dict(o=FAKE + 64), FA_ERR_INVALID_ARGUMENT),         # output overlaps q
+    (dict(B=1 << 14, H=1 << 10, N=1 << 10), FA_ERR_INVALID_ARGUMENT),  # too many elements
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _bwd(lib, *, ws=None, ws_bytes=0, dq=FAKE + (10 << 30), B=1, H=2, N=128, d=64, causal=0, scale=0.125,
+         lse=FAKE + (5 << 30)):
+    return lib.fa_bwd(FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30), FAKE + (4 << 30), lse,
+                      dq, FAKE + (11 << 30), FAKE + (12 << 30), B, H, N, d, causal, scale, ws, ws_bytes, None)
+
+
+def test_bwd_rejects(lib):
+    assert _bwd(lib, d=80) == FA_ERR_UNSUPPORTED
+    assert _bwd(lib, N=-3) == FA_ERR_INVALID_ARGUMENT
+    assert _bwd(lib, scale=float("nan")) == FA_ERR_INVALID_ARGUMENT
+    assert _bwd(lib, dq=FAKE + 16) == FA_ERR_INVALID_ARGUMENT        # dq overlaps q
+    assert _bwd(lib, lse=0) == FA_ERR_INVALID_ARGUMENT
+    need = lib.fa_bwd_workspace_bytes(1, 2, 128, 64)
+    assert _bwd(lib, ws=FAKE + (20 << 30), ws_bytes=need - 1) == FA_ERR_WORKSPACE
+    assert _bwd(lib, ws=FAKE + (20 << 30) + 16, ws_bytes=need) == FA_ERR_INVALID_ARGUMENT  # not 256-aligned
+    assert _bwd(lib, ws=FAKE + (3 << 30), ws_bytes=need) == FA_ERR_INVALID_ARGUMENT        # overlaps o
+
+
+def test_workspace_bytes(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for B, H, N, d in [(1, 2, 128, 64), (2, 16, 8192, 128), (1, 1, 1, 64), (3, 5, 129, 128)]:
+        Np = (N + 127) // 128 * 128
+        want = r256(B * H * N * d * 4) + 2 * r256(B * H * Np * 4)
+        assert lib.fa_bwd_workspace_bytes(B, H, N, d) == want
+    # linear in N (the pages' O(N) memory claim), not quadratic
+    a = lib.fa_bwd_workspace_bytes(1, 1, 4096, 128)
+    b = lib.fa_bwd_workspace_bytes(1, 1, 8192, 128)
+    assert b == 2 * a
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 96) == 0
+    assert lib.fa_bwd_workspace_bytes(0, 1, 128, 64) == 0

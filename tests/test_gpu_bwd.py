@@ -1,0 +1,93 @@
+"""Backward parity: fa_bwd (CUDA, through the C ABI) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_48_gb300 import fa_bwd, fa_bwd_workspace_bytes, fa_device_status, fa_fwd
+from exact_attention_48_gb300.inputs import draw_shape
+from parity import check_grad
+
+pytestmark = pytest.mark.gpu
+
+SMALL_N = [1, 64, 127, 128, 129, 200, 256, 384]
+
+
+def _run(B, H, N, d, causal, scale=None, seed=7, mult=1.0, workspace=False):
+    q, k, v, do = draw_shape(B, H, N, d, seed, mult, "cpu", torch.bfloat16)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa_fwd(qc, kc, vc, causal, scale)
+    dq = torch.full_like(qc, float("nan"))
+    dk = torch.full_like(qc, float("nan"))
+    dv = torch.full_like(qc, float("nan"))
+    ws = None
+    if workspace:
+        ws = torch.full((fa_bwd_workspace_bytes(B, H, N, d),), 0x7F, dtype=torch.uint8, device="cuda")
+    fa_bwd(qc, kc, vc, o, doc, lse, causal, scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+    assert fa_device_status() == 0
+    ref = oracle.bwd(q, k, v, do, causal, scale)
+    return (dq, dk, dv), ref
+
+
+def _check(got, ref, what):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        check_grad(g, r, name, what)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", SMALL_N)
+def test_bwd_small(N, d, causal):
+    got, ref = _run(2, 2, N, d, causal, seed=200 + N + d)
+    _check(got, ref, f"N={N} d={d} causal={causal}")
+
+
+def test_bwd_caller_workspace_and_reuse():
+    """A caller workspace filled with garbage gives the same result as the
+    library's own allocation, and it can be reused call after call."""
+    got1, ref = _run(1, 3, 300, 128, True, seed=5, workspace=True)
+    _check(got1, ref, "caller workspace")
+    got2, _ = _run(1, 3, 300, 128, True, seed=5, workspace=False)
+    for a, b in zip(got1[1:], got2[1:]):   # dk, dv have no atomics: identical
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_bwd_scale_values(scale):
+    got, ref = _run(1, 2, 200, 64, True, scale=scale, seed=9)
+    _check(got, ref, f"scale={scale}")
+
+
+def test_bwd_gradient_identities():
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold on the GPU results too."""
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, do = draw_shape(B, H, N, d, 21, 1.0, "cuda", torch.bfloat16)
+    o, lse = fa_fwd(q, k, v, True)
+    dq, dk, dv = fa_bwd(q, k, v, o, do, lse, True)
+    torch.cuda.synchronize()
+    sdk = dk.double().sum(2)
+    assert float(sdk.abs().max()) <= 2e-2 * float(dk.double().abs().max()) * math.sqrt(N)
+    sdv = dv.double().sum(2)
+    sdo = do.double().sum(2)
+    assert float((sdv - sdo).abs().max()) <= 2e-2 * float(sdo.abs().max()) + 0.05
+
+
+def test_bwd_guard_bands():
+    B, H, N, d = 1, 2, 200, 64
+    q, k, v, do = draw_shape(B, H, N, d, 5, 1.0, "cuda", torch.bfloat16)
+    o, lse = fa_fwd(q, k, v, False)
+    pad = 4096
+    n = B * H * N * d
+    bufs = [torch.full((n + 2 * pad,), 3.0, device="cuda", dtype=torch.bfloat16) for _ in range(3)]
+    wsn = fa_bwd_workspace_bytes(B, H, N, d)
+    wsb = torch.full((wsn + 2 * 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = wsb[4096:4096 + wsn]
+    views = [b[pad:pad + n].view(B, H, N, d) for b in bufs]
+    fa_bwd(q, k, v, o, do, lse, False, dq=views[0], dk=views[1], dv=views[2], workspace=ws)
+    torch.cuda.synchronize()
+    for b in bufs:
+        assert torch.all(b[:pad] == 3) and torch.all(b[-pad:] == 3)
+    assert torch.all(wsb[:4096] == 0x5A) and torch.all(wsb[-4096:] == 0x5A)

@@ -1,0 +1,82 @@
+"""Forward parity: fa_fwd (CUDA, through the C ABI) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_48_gb300 import fa_fwd, fa_device_status
+from exact_attention_48_gb300.inputs import draw_shape
+from parity import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+SMALL_N = [1, 64, 127, 128, 129, 200, 256, 384]
+
+
+def _run(B, H, N, d, causal, scale=None, seed=7, mult=1.0):
+    q, k, v, _ = draw_shape(B, H, N, d, seed, mult, "cpu", torch.bfloat16, with_dout=False)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qc, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), device="cuda")
+    fa_fwd(qc, kc, vc, causal, scale, o=o, lse=lse)
+    assert fa_device_status() == 0
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal, scale)
+    return o, lse, o_ref, lse_ref
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", SMALL_N)
+def test_fwd_small(N, d, causal):
+    o, lse, o_ref, lse_ref = _run(2, 2, N, d, causal, seed=100 + N + d)
+    check_o(o, o_ref, f"N={N} d={d} causal={causal}")
+    check_lse(lse, lse_ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 0.5])
+def test_fwd_scale_values(scale):
+    for causal in (False, True):
+        o, lse, o_ref, lse_ref = _run(1, 2, 200, 64, causal, scale=scale, seed=3)
+        check_o(o, o_ref, f"scale={scale}")
+        check_lse(lse, lse_ref, f"scale={scale}")
+
+
+def test_fwd_deterministic():
+    q, k, v, _ = draw_shape(2, 4, 1000, 128, 11, 1.0, "cuda", torch.bfloat16, with_dout=False)
+    o1, l1 = fa_fwd(q, k, v, True)
+    for _ in range(3):
+        o2, l2 = fa_fwd(q, k, v, True)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fwd_guard_bands():
+    """Writes stay inside o and lse: canaries around both survive."""
+    B, H, N, d = 1, 3, 300, 64
+    q, k, v, _ = draw_shape(B, H, N, d, 5, 1.0, "cuda", torch.bfloat16, with_dout=False)
+    pad = 4096
+    ob = torch.full((B * H * N * d + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
+    lb = torch.full((B * H * N + 2 * pad,), 7.0, device="cuda")
+    o = ob[pad:pad + B * H * N * d].view(B, H, N, d)
+    lse = lb[pad:pad + B * H * N].view(B, H, N)
+    fa_fwd(q, k, v, False, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(ob[:pad] == 7) and torch.all(ob[-pad:] == 7)
+    assert torch.all(lb[:pad] == 7) and torch.all(lb[-pad:] == 7)
+
+
+def test_fwd_constant_v_and_zero_q():
+    B, H, N, d = 1, 2, 333, 128
+    q, k, v, _ = draw_shape(B, H, N, d, 9, 1.0, "cuda", torch.bfloat16, with_dout=False)
+    c = torch.randn(d, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).cuda()
+    vc = c.expand(B, H, N, d).contiguous()
+    for causal in (False, True):
+        o, _ = fa_fwd(q, k, vc, causal)
+        assert torch.allclose(o.float(), vc.float(), atol=2e-2, rtol=0)
+    z = torch.zeros_like(q)
+    o, lse = fa_fwd(z, k, v, False)
+    mean = v.double().mean(2, keepdim=True).expand_as(o)
+    assert torch.allclose(o.double(), mean, atol=1e-2)
+    assert torch.allclose(lse.double(), torch.full_like(lse.double(), math.log(N)), atol=1e-3)
