@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Attention fwd+bwd TFLOP/s on one GB300 (and N GPUs as independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: fa_fwd (O, logsumexp)
+then fa_bwd (dQ, dK, dV) on the headline workload B=2, H=16, N=8192, d=128,
+non-causal, bf16 inputs drawn i.i.d. N(0,1) from a fixed seed.  FLOPs per
+step: 4*B*H*N^2*d forward + 2.5x that backward.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead: each
+step is fwd+bwd of a bounded sample of query rows of one head (all keys),
+sized so the whole run stays within a few minutes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s at 1 GB300 and fraction of BF16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--causal", action="store_true", help="time the causal variant of the workload")
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload(args):
+    from exact_attention_48_gb300.inputs import sweep
+    return sweep(args.N, args.d, args.causal)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {k: float(j[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1 + 0.25:
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, rows, seed_offset=0, nthreads=None):
+    """Time the oracle on `rows` query rows of head (0, 0) against all keys.
+
+    Returns (seconds, flops, threads).  FLOPs are counted like the GPU's:
+    4*rows*N*d forward and 2.5x that backward (non-causal sample)."""
+    import torch
+    import oracle
+    from exact_attention_48_gb300.inputs import draw_shape
+    q, k, v, do = draw_shape(1, 1, w.N, w.d, w.seed + seed_offset, w.input_mult, "cpu", torch.bfloat16)
+    q, do = q[:, :, :rows], do[:, :, :rows]
+    nt = nthreads or oracle.default_threads()
+    qn, kn, vn, don = (oracle._f64(x) for x in (q, k, v, do))
+    t0 = time.perf_counter()
+    oracle.fwd(qn, kn, vn, False, w.scale, nthreads=nt)
+    oracle.bwd(qn, kn, vn, don, False, w.scale, nthreads=nt)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * rows * w.N * w.d * 3.5
+    return dt, flops, nt
+
+
+def cpu_baseline(w, target_s=12.0):
+    # calibrate on a small sample, then size the timed one to ~target_s
+    dt, fl, nt = oracle_sample(w, 64)
+    rate = fl / max(dt, 1e-6)
+    rows = int(min(w.N, max(64, target_s * rate / (4.0 * w.N * w.d * 3.5))))
+    rows = max(64, rows // 64 * 64)
+    dt, fl, nt = oracle_sample(w, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+            "sample": f"fwd+bwd of query rows 0..{rows - 1} of head (0,0) against all {w.N} keys, "
+                      f"d={w.d}, non-causal, fp64 C oracle, {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    w = workload(args)
+    # size each step so that warmup + steps take about 100 s in all
+    dt, fl, nt = oracle_sample(w, 64)
+    rate = fl / max(dt, 1e-6)
+    per_step_s = max(0.5, min(10.0, 100.0 / max(1, args.steps + args.warmup)))
+    rows = int(min(w.N, max(16, per_step_s * rate / (4.0 * w.N * w.d * 3.5))))
+    for i in range(args.warmup):
+        oracle_sample(w, rows, i + 1, nt)
+    t_total, fl_total = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl, _ = oracle_sample(w, rows, 1000 + i, nt)
+        t_total += dt
+        fl_total += fl
+    value = fl_total / t_total / 1e12
+    sample = (f"per step: fwd+bwd of {rows} query rows of one head against all {w.N} keys, d={w.d}, "
+              f"non-causal, fp64 C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ multi-rank
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(flops_per_step_per_rank: float, steps: int, local_ms: float, world: int,
+                         device=None) -> tuple[float, float]:
+    """Whole-job TFLOP/s (every rank runs its own batch) and the max-over-ranks time in ms."""
+    ms = reduce_max(local_ms, device)
+    return world * flops_per_step_per_rank * steps / (ms * 1e-3) / 1e12, ms
+
+
+# ------------------------------------------------------------------ GPU
+
+def config_of(w):
+    return {"workload": f"fwd+bwd B{w.B} H{w.H} N{w.N} d{w.d} {'causal' if w.causal else 'non-causal'} bf16",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
+            "inputs": f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}",
+            "l2": "no flush: the tensors touched per step (q,k,v,o,dO,dq,dk,dv + fp32 dQ accumulator) "
+                  "are several times larger than the 129 MB L2"}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since those counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if h != rec.get("source_sha256_16"):
+        return None
+    if rec.get("workload") != rec.get("bench_workload"):
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from exact_attention_48_gb300 import fa_bwd, fa_bwd_workspace_bytes, fa_device_status, fa_fwd
+    from exact_attention_48_gb300.binding import fa_debug_time_next_bwd_main
+    from exact_attention_48_gb300.inputs import draw
+
+    w = workload(args)
+    # every rank runs its own batch (independent heads): weak scaling, no data-path collective
+    q, k, v, do = draw(w, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
+        if evs is not None:
+            evs[1].record(stream)
+            fa_debug_time_next_bwd_main(evs[2], evs[3])
+        fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(max(args.warmup, 3 if args.warmup >= 3 else args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa_device_status() != 0:
+        raise SystemExit("device status error after warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)  # let the sampler start
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    if fa_device_status() != 0:
+        raise SystemExit("device status error in the timed region")
+
+    flops_step = w.flops_fwd() + w.flops_bwd()
+    value, elapsed_ms = aggregate_throughput(flops_step, args.steps, start.elapsed_time(stop), world, "cuda")
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
+    bwd_main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    peaks, peak_src = load_peaks()
+    peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
+    fwd_tf = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12
+    bwd_main_tf = w.flops_bwd() / (bwd_main_ms * 1e-3) / 1e12
+    # dominant kernel: the backward main kernel (the forward kernel is timed beside it)
+    dom, dom_ms, dom_tf = ("fa_bwd_main_kernel", bwd_main_ms, bwd_main_tf) if bwd_main_ms >= fwd_ms else \
+        ("fa_fwd_kernel", fwd_ms, fwd_tf)
+    traffic = traffic_record(dom)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w),
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_sustained": fwd_tf / peak_sus,
+                "frac_of_burst": fwd_tf / peak_burst},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_sustained": bwd_tf / peak_sus,
+                "frac_of_burst": bwd_tf / peak_burst, "main_kernel_ms": bwd_main_ms},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": dom_tf,
+                     "peak": peak_sus, "unit": "TFLOP/s", "frac": dom_tf / peak_sus,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "traffic": traffic},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
+    """Same metric through the public API from HOST buffers: every step copies
+    q, k, v, dO from pinned host memory to the device and o, lse, dq, dk, dv
+    back, inside the timed region."""
+    import torch
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+    outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4)]
+    hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    q_, k_, v_, do_ = (torch.empty_like(q) for _ in range(4))
+    o_ = torch.empty_like(q)
+    lse_ = torch.empty((w.B, w.H, w.N), device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+            dst.copy_(src, non_blocking=True)
+        fa_fwd(q_, k_, v_, w.causal, w.scale, o=o_, lse=lse_)
+        fa_bwd(q_, k_, v_, o_, do_, lse_, w.causal, w.scale, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
+        for dst, src in zip(outs, (o_, dq_, dk_, dv_)):
+            dst.copy_(src, non_blocking=True)
+        hlse.copy_(lse_, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    flops = w.flops_fwd() + w.flops_bwd()
+    value, ms = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
+    nbytes = q.numel() * q.element_size()
+    return {"value": value, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes + hlse.numel() * 4,
+            "steps": steps}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

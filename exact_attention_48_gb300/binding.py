@@ -59,6 +59,8 @@ def library(path: str | None = None):
             lib.fa_device_status.restype = i
             lib.fa_debug_last_wait_site.argtypes = []
             lib.fa_debug_last_wait_site.restype = i
+            lib.fa_debug_time_next_bwd_main.argtypes = [vp, vp]
+            lib.fa_debug_time_next_bwd_main.restype = i
             lib.fa_status_string.argtypes = [i]
             lib.fa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -150,6 +152,15 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_debug_time_next_bwd_main(start: "torch.cuda.Event", stop: "torch.cuda.Event") -> None:
+    """Have the next fa_bwd of this thread record the two events around its main kernel."""
+    start.record()  # make sure torch has created the underlying CUDA events
+    stop.record()
+    rc = library().fa_debug_time_next_bwd_main(start.cuda_event, stop.cuda_event)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_debug_time_next_bwd_main")
 
 
 def fa_device_status(stream=None) -> int:

@@ -67,6 +67,9 @@ fa_status_t check_common(int B, int H, int N, int d, int causal, float scale) {
   return FA_OK;
 }
 
+// Events the next fa_bwd call of this thread records around its main kernel.
+thread_local cudaEvent_t t_bwd_ev_start = nullptr, t_bwd_ev_stop = nullptr;
+
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -186,7 +189,9 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status_t rc = FA_OK;
-  if (!p.status || launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream) != cudaSuccess) rc = FA_ERR_CUDA;
+  cudaEvent_t ev0 = t_bwd_ev_start, ev1 = t_bwd_ev_stop;
+  t_bwd_ev_start = t_bwd_ev_stop = nullptr;
+  if (!p.status || launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream, ev0, ev1) != cudaSuccess) rc = FA_ERR_CUDA;
   if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   return rc;
 }
@@ -200,6 +205,13 @@ fa_status_t fa_device_status(cudaStream_t stream) {
     if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
     return static_cast<fa_status_t>(h[0]);
   }
+  return FA_OK;
+}
+
+fa_status_t fa_debug_time_next_bwd_main(cudaEvent_t start, cudaEvent_t stop) {
+  if (!start || !stop) return FA_ERR_INVALID_ARGUMENT;
+  t_bwd_ev_start = start;
+  t_bwd_ev_stop = stop;
   return FA_OK;
 }
 

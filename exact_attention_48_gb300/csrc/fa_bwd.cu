@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
-                         const BwdParams &p, cudaStream_t stream) {
+                         const BwdParams &p, cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   using L = BwdLayout<D>;
   const long long rows = static_cast<long long>(p.BH) * p.N;
   const long long padded_rows = static_cast<long long>(p.BH) * p.num_blk * kBlk;
@@ -488,10 +488,12 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   auto kern = fa_bwd_main_kernel<D, CAUSAL>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return e;
+  if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk), 384, L::kSmemRequest, stream>>>(tq, tk, tv,
                                                                                                        tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return e;
 
   const long long n4 = rows * D / 4;
   long long blocks = (n4 + 255) / 256;
@@ -503,10 +505,13 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream) {
+                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, cudaEvent_t ev_start,
+                       cudaEvent_t ev_stop) {
   if (d == 64)
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream) : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream);
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream) : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream);
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop);
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop);
 }
 
 }  // namespace fa

@@ -62,8 +62,9 @@ struct BwdParams {
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 
+// ev_start/ev_stop (may be null) are recorded around the main kernel.
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
-                       cudaStream_t stream);
+                       cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace fa

@@ -120,6 +120,17 @@ FA_API fa_status_t fa_device_status(cudaStream_t stream);
  */
 FA_API int fa_debug_last_wait_site(void);
 
+/*
+ * Diagnostic timing hook: the next fa_bwd call made by this host thread
+ * records `start` on its stream right before the launch of its main kernel
+ * (the one that recomputes the probabilities and forms dQ, dK, dV) and
+ * `stop` right after it, so that kernel can be timed with
+ * cudaEventElapsedTime.  The events are created and owned by the caller;
+ * the hook is used once and then cleared.  Returns FA_ERR_INVALID_ARGUMENT
+ * if either event is NULL.
+ */
+FA_API fa_status_t fa_debug_time_next_bwd_main(cudaEvent_t start, cudaEvent_t stop);
+
 /* A static, NUL-terminated description of a status code. */
 FA_API const char *fa_status_string(fa_status_t status);
 

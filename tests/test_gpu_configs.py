@@ -1,0 +1,103 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py uses.
+
+For each workload the whole tensors go through fa_fwd / fa_bwd once; the fp64
+oracle then recomputes a fixed subset of heads (first, last and two seeded
+ones) completely, all rows and all columns.  A secondary check compares every
+head against PyTorch fp32 attention on the GPU (a library routine, upcast
+from the same bf16 inputs).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_48_gb300 import fa_bwd, fa_device_status, fa_fwd
+from exact_attention_48_gb300.inputs import (CAUSAL_B4H32N4096D128, FWD_B8H16N2048D64, LONG_B1H16N16384D128,
+                                             TINY, draw, sweep)
+from parity import check_grad, check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def heads_to_check(B, H, n_extra=2, max_heads=4):
+    BH = B * H
+    r = np.random.default_rng(BH)
+    picks = {0, BH - 1}
+    while len(picks) < min(BH, 2 + n_extra):
+        picks.add(int(r.integers(0, BH)))
+    return sorted(picks)[:max_heads]
+
+
+def _torch_ref_fwd(q, k, v, causal, scale):
+    """fp32 GPU reference, one head at a time (O and LSE)."""
+    B, H, N, d = q.shape
+    o = torch.empty(B, H, N, d, device=q.device, dtype=torch.float32)
+    lse = torch.empty(B, H, N, device=q.device, dtype=torch.float32)
+    mask = torch.ones(N, N, device=q.device, dtype=torch.bool).triu(1) if causal else None
+    for b in range(B):
+        for h in range(H):
+            s = (q[b, h].float() @ k[b, h].float().T) * scale
+            if causal:
+                s.masked_fill_(mask, float("-inf"))
+            lse[b, h] = torch.logsumexp(s, -1)
+            o[b, h] = torch.softmax(s, -1) @ v[b, h].float()
+            del s
+    return o, lse
+
+
+def _run(w, heads_max=4, full_torch=True):
+    q, k, v, do = draw(w, device="cuda")
+    o, lse = fa_fwd(q, k, v, w.causal, w.scale)
+    grads = None
+    if w.backward:
+        grads = fa_bwd(q, k, v, o, do, lse, w.causal, w.scale)
+    assert fa_device_status() == 0
+    torch.cuda.synchronize()
+    heads = heads_to_check(w.B, w.H, max_heads=heads_max)
+    qf, kf, vf, dof = (t.view(w.B * w.H, w.N, w.d) for t in (q, k, v, do))
+    of, lsef = o.view(w.B * w.H, w.N, w.d), lse.view(w.B * w.H, w.N)
+    for hh in heads:
+        o_ref, lse_ref = oracle.fwd(qf[hh], kf[hh], vf[hh], w.causal, w.scale)
+        check_o(of[hh], o_ref, f"{w.name} head {hh}")
+        check_lse(lsef[hh], lse_ref, f"{w.name} head {hh}")
+        if grads is not None:
+            refs = oracle.bwd(qf[hh], kf[hh], vf[hh], dof[hh], w.causal, w.scale)
+            for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+                check_grad(g.view(w.B * w.H, w.N, w.d)[hh], r, name, f"{w.name} head {hh}")
+    if full_torch:
+        o_t, lse_t = _torch_ref_fwd(q, k, v, w.causal, w.scale)
+        err = (o.float() - o_t).abs()
+        bound = torch.clamp(0.5 * torch.exp2(torch.floor(torch.log2(o_t.abs().clamp_min(1e-30)))) / 128 + 2e-3,
+                            min=1e-2)
+        assert bool((err <= bound + 1e-6).all()), f"{w.name}: O vs torch fp32, max err {float(err.max()):.3e}"
+        assert float((lse - lse_t).abs().max()) <= 1e-3
+    return q, k, v, o, lse
+
+
+def test_tiny_workload():
+    _run(TINY)
+
+
+def test_forward_only_b8h16n2048d64():
+    _run(FWD_B8H16N2048D64)
+
+
+def test_causal_b4h32n4096d128():
+    _run(CAUSAL_B4H32N4096D128, heads_max=3)
+
+
+def test_long_context_b1h16n16384d128():
+    _run(LONG_B1H16N16384D128, heads_max=2, full_torch=False)
+
+
+@pytest.mark.parametrize("N", [512, 2048, 8192, 16384])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_points_d128(N, causal):
+    _run(sweep(N, 128, causal), heads_max=2, full_torch=(N <= 8192))
+
+
+@pytest.mark.parametrize("N", [512, 4096])
+def test_sweep_points_d64(N):
+    _run(sweep(N, 64, True), heads_max=2)
