@@ -119,7 +119,7 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
   p.BH = BH;
-  p.num_qblk = (N + 127) / 128;
+  p.num_qblk = (N + 255) / 256;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.neg = scale < 0.0f ? 1 : 0;
   return launch_fwd(d, causal != 0, tq, tk, tv, p, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;

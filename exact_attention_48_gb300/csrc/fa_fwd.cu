@@ -1,26 +1,31 @@
 // fa_fwd.cu -- forward kernel of exact attention for sm_103a.
 //
-// One CTA owns 128 query rows of one (batch, head) and walks the key/value
-// blocks of that head (lexicon page "FlashAttention" (urworte.de), section
-// "Methodische Grundlagen": block-wise processing in on-chip memory, the
-// score / normalisation / weighting steps fused in one pass, and a running
-// row normalisation that corrects the partial output whenever a larger
-// score appears).  The grid spreads the query blocks of every head over the
-// SMs (page "FlashAttention-2 (DE)", "Technische Architektur", section 2).
+// One CTA owns 256 query rows (two tiles of 128) of one (batch, head) and
+// walks the key/value blocks of that head (lexicon page "FlashAttention"
+// (urworte.de), section "Methodische Grundlagen": block-wise processing in
+// on-chip memory, the score / normalisation / weighting steps fused in one
+// pass, and a running row normalisation that corrects the partial output
+// whenever a larger score appears).  The grid spreads the query blocks of
+// every head over the SMs (page "FlashAttention-2 (DE)", "Technische
+// Architektur", section 2).
 //
-// Roles inside the CTA (256 threads):
-//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of stages
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into TMEM, O += P_j V_j
-//   warp 2      owns the TMEM allocation
-//   warps 4..7  softmax: one query row per thread, running max m and sum l
-//               in registers, P_j written back as bf16 over S_j in TMEM
-//               (it is the A operand of the P V product), O rescaled in TMEM
-//               when m grows, final O / l and the logsumexp.
+// Roles inside the CTA (384 threads, three warpgroups):
+//   warps 0..3   softmax of tile 0, warps 4..7 softmax of tile 1: one query
+//                row per thread, running max m and sum l in registers, P
+//                written back as bf16 over S in TMEM (it is the A operand of
+//                the P V product), O rescaled in TMEM when m grows, final
+//                O / l and the logsumexp.
+//   warp 8       TMA producer: both Q tiles once, then K_j and V_j into a
+//                ring of stages
+//   warp 9       MMA issuer (one thread): S_t = Q_t K_j^T into TMEM and
+//                O_t += P_t V_j for both tiles t, interleaved so that the
+//                tensor core works on one tile while the other is
+//                normalised; the warp also owns the TMEM allocation.
+//   warps 10, 11 idle (they complete the third warpgroup).
 //
-// TMEM columns: S_0 [0,128), S_1 [128,256), O [256, 256+d).  Two S buffers
-// let the score product of block j+1 run while rows of block j are being
-// normalised.  Only scores and probabilities of the current block ever
-// exist, and only on chip (page "FlashAttention-2 (DE)", "Hintergrund").
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d),
+// O_1 [256+d, 256+2d).  Only scores and probabilities of the current block
+// ever exist, and only on chip (page "FlashAttention-2 (DE)", "Hintergrund").
 //
 // Scores are kept in the log2 domain: t = s * scale * log2(e).  The running
 // max is only moved when a row's new block max exceeds it by more than 8
@@ -34,19 +39,20 @@ namespace fa {
 
 namespace {
 
-constexpr int kBM = 128;  // query rows per CTA
+constexpr int kBM = 128;  // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;  // keys per block
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct FwdLayout {
   static constexpr int kSlabs = D / 64;  // 128-byte column slabs of a bf16 row
-  static constexpr int kStages = (D == 64) ? 4 : 3;
-  static constexpr uint32_t kQBytes = kBM * D * 2;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr uint32_t kQTile = kBM * D * 2;
   static constexpr uint32_t kKVBytes = kBN * D * 2;
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kQBytes;
+  static constexpr uint32_t kOffQ = 0;  // two tiles
+  static constexpr uint32_t kOffK = kOffQ + 2 * kQTile;
   static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2], pv_done[2], drain
@@ -57,10 +63,184 @@ struct FwdLayout {
   static_assert(kSmemRequest <= 232448, "shared memory budget");
 };
 
-constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 384;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+// Register split: 168 per thread at launch (384 x 168 fits the SM); the
+// control warpgroup gives back down to 104 and the two softmax warpgroups
+// take 200 each: 128*104 + 256*200 <= 384*168, and per SM sub-partition
+// (one warp of each warpgroup) 32*(104 + 2*200) <= 16384.
+constexpr uint32_t kRegsLaunch = 168, kRegsControl = 104, kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+
+struct SoftmaxArgs {
+  uint64_t *s_full, *p_ready, *pv_done;
+  uint32_t tS, tO;  // TMEM columns of this tile's S and O (lane base added inside)
+  int n_kv;         // key blocks this tile visits
+  int diag;         // causal: index of the diagonal key block, else -1
+  int grow0;        // first query row of the tile
+};
+
+// Online softmax of one 128-row tile: one query row per thread.
+template <int D>
+__device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdParams &p, const WaitCtl &ctl, int bh,
+                                             int warp, int lane) {
+  const int wq = warp & 3;
+  const int row = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const int N = p.N;
+  const float c = p.scale_log2;
+  const bool neg = p.neg != 0;
+  const uint32_t tS = a.tS + lane_base, tO = a.tO + lane_base;
+  float m_run = -INFINITY, l_run = 0.0f, lb_run = 0.0f;
+  bool ok = true;
+
+  for (int j = 0; j < a.n_kv; ++j) {
+    ok = mbar_wait(a.s_full, j & 1, ctl, kSiteSFull);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t s[4][32];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, s[q4]);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(s[q4]);
+
+    // Masking: causal diagonal block and the ragged last key block.
+    const bool need_mask = (j == a.diag) || ((j + 1) * kBN > N);
+    int lim = kBN - 1;  // last visible column of this row
+    if (need_mask) {
+      lim = min(lim, N - 1 - j * kBN);
+      if (j == a.diag) lim = min(lim, row);
+      const uint32_t hide = __float_as_uint(neg ? INFINITY : -INFINITY);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (q4 * 32 + i > lim) s[q4][i] = hide;
+    }
+
+    // Block max of t = s * c (a min of s when the scale is negative).
+    float mx;
+    if (!neg) {
+      float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          m0 = fmax3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
+          m1 = fmax3(m1, __uint_as_float(s[q4][i + 2]), __uint_as_float(s[q4][i + 3]));
+        }
+      mx = fmaxf(m0, m1);
+    } else {
+      float m0 = INFINITY, m1 = INFINITY;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          m0 = fmin3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
+          m1 = fmin3(m1, __uint_as_float(s[q4][i + 2]), __uint_as_float(s[q4][i + 3]));
+        }
+      mx = fminf(m0, m1);
+    }
+    const float m_cand = mx * c;
+    const bool grow = m_cand > m_run + kRescaleThreshold;
+    float alpha = 1.0f;
+    if (grow) {
+      alpha = ex2(m_run - m_cand);
+      m_run = m_cand;
+    }
+    l_run *= alpha;
+    lb_run *= alpha;
+    const float2 cc = make_float2(c, c), nm = make_float2(-m_run, -m_run);
+
+    // P = exp2(t - m) as bf16 pairs over the first 64 columns of S, one
+    // quarter (32 keys -> 16 columns) at a time to keep few values live.
+    // Two row sums: of the fp32 P (for the logsumexp) and of the bf16 P the
+    // P V product uses (for O, so the weights applied to V add up to one).
+    float2 sf = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 x = ffma2(make_float2(__uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1])), cc, nm);
+        float p0 = ex2(x.x), p1 = ex2(x.y);
+        if (need_mask) {
+          p0 = (q4 * 32 + i <= lim) ? p0 : 0.0f;
+          p1 = (q4 * 32 + i + 1 <= lim) ? p1 : 0.0f;
+        }
+        const uint32_t b = pack_bf16x2(p0, p1);
+        pk[i / 2] = b;
+        sf = fadd2(sf, make_float2(p0, p1));
+        sb = fadd2(sb, make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
+      }
+      tmem_st16(tS + q4 * 16, pk);
+    }
+    const float sum0 = sf.x, sum1 = sf.y;
+    lb_run += sb.x + sb.y;
+    l_run += sum0 + sum1;
+    tmem_st_wait();
+
+    // O of the previous block must be complete before it is rescaled and
+    // before the next product accumulates into it.
+    if (j > 0) {
+      ok = mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, grow)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + ch * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + ch * 32, o);
+        }
+        tmem_st_wait();
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(a.p_ready);
+  }
+
+  // Epilogue: O / l in bf16 and the natural-log logsumexp.
+  if (ok) {
+    ok = mbar_wait(a.pv_done, (a.n_kv - 1) & 1, ctl, kSitePvDone);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  if (ok) {
+    tc_fence_after();
+    const float inv_l = 1.0f / lb_run;
+    const int grow_row = a.grow0 + row;
+    const bool store = grow_row < N;
+    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + grow_row) * D;
+#pragma unroll 1
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t o[32];
+      tmem_ld32(tO + ch * 32, o);
+      tmem_ld_wait(o);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (store) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    if (store) p.lse[static_cast<size_t>(bh) * N + grow_row] = (m_run + log2f(l_run)) * kLn2;
+  }
+}
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = FwdLayout<D>;
@@ -74,9 +254,9 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t *k_empty = k_full + S;
   uint64_t *v_full = k_empty + S;
   uint64_t *v_empty = v_full + S;
-  uint64_t *s_full = v_empty + S;
-  uint64_t *p_ready = s_full + 2;
-  uint64_t *pv_done = p_ready + 2;
+  uint64_t *s_full = v_empty + S;   // [2 tiles]
+  uint64_t *p_ready = s_full + 2;   // [2 tiles]
+  uint64_t *pv_done = p_ready + 2;  // [2 tiles]
   uint64_t *drain = pv_done + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
@@ -85,19 +265,22 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Tile order.  Causal: the heaviest query blocks (most key blocks) first,
-  // across all heads.  Otherwise head-major so that CTAs running together
-  // share the K/V of one head in L2.
-  int bh, qblk;
+  // Tile order.  Causal: the heaviest 256-row blocks (most key blocks)
+  // first, across all heads.  Otherwise head-major so that CTAs running
+  // together share the K/V of one head in L2.
+  int bh, qb;
   if (CAUSAL) {
-    qblk = p.num_qblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    qb = p.num_qblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
     bh = static_cast<int>(blockIdx.x) % p.BH;
   } else {
     bh = static_cast<int>(blockIdx.x) / p.num_qblk;
-    qblk = static_cast<int>(blockIdx.x) % p.num_qblk;
+    qb = static_cast<int>(blockIdx.x) % p.num_qblk;
   }
   const int N = p.N;
-  const int n_kv = CAUSAL ? (qblk + 1) : (N + kBN - 1) / kBN;
+  const int nkv_all = (N + kBN - 1) / kBN;
+  const int n0 = CAUSAL ? min(2 * qb + 1, nkv_all) : nkv_all;  // key blocks of tile 0
+  const int n1 = CAUSAL ? min(2 * qb + 2, nkv_all) : nkv_all;  // key blocks of tile 1 (>= n0)
+  const int n_kv = n1;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -107,16 +290,16 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_ready[b], 128);
-      mbar_init(&pv_done[b], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_ready[t], 128);
+      mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -124,21 +307,24 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
 
   uint8_t *sQ = smem + L::kOffQ;
   uint8_t *sK = smem + L::kOffK;
   uint8_t *sV = smem + L::kOffV;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp >= kWarpProducer) {
+    regs_decrease<kRegsControl>();
+    if (warp == kWarpProducer && lane == 0) {
+      // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(q_full, L::kQBytes);
+      mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
 #pragma unroll
-      for (int s = 0; s < L::kSlabs; ++s) tma_load_3d(sQ + s * kBM * 128, &tm_q, q_full, s * 64, qblk * kBM, bh);
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int s = 0; s < L::kSlabs; ++s)
+          tma_load_3d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, qb * 2 * kBM + t * kBM, bh);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
@@ -162,215 +348,91 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = (k_issued > S ? k_issued - S : 0); j < k_issued; ++j) mbar_drain(&k_full[j % S], (j / S) & 1);
         for (int j = (v_issued > S ? v_issued - S : 0); j < v_issued; ++j) mbar_drain(&v_full[j % S], (j / S) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16(kBM, D, false, true);
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
+      // TMEM columns of tile t: S at t*128, O at 256 + t*D
 
-      // O += P_t V_t; P_t sits (bf16, two per column) over S_t in TMEM.
-      auto issue_pv = [&](int t) -> bool {
-        const int b = t & 1, st = t % S;
-        if (!mbar_wait(&p_ready[b], (t >> 1) & 1, ctl, kSitePReady)) return false;
-        if (!mbar_wait(&v_full[st], (t / S) & 1, ctl, kSiteVFull)) return false;
-        tc_fence_after();
-        const uint32_t vbase = aV + st * L::kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // V_t is [key][d]: MN-major for this product (d contiguous).  16
-          // keys = two 8-row groups of 1024 bytes; d slabs 128*128 bytes apart.
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, kBN * 128, 1024);
-          mma_ts(tO, tS0 + b * 128 + kk * 8, bdesc, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&v_empty[st]);
-        tc_commit(&pv_done[b]);
-        return true;
-      };
-
-      bool ok = mbar_wait(q_full, 0, ctl, kSiteQFull);
-      tc_fence_after();
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % S, b = j & 1;
-        if (!mbar_wait(&k_full[st], (j / S) & 1, ctl, kSiteKFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = aK + st * L::kKVBytes;
+      // S_t = Q_t K_j^T (both operands K-major over d)
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kbase = aK + (j % S) * L::kKVBytes, qbase = aQ + t * L::kQTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint64_t adesc = sdesc_sw128(aQ + koff, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(kbase + koff, 16, 1024);
-          mma_ss(tS0 + b * 128, adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + t * 128, sdesc_sw128(qbase + koff, 16, 1024), sdesc_sw128(kbase + koff, 16, 1024), kIdescS,
+                 kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[b]);
-        tc_commit(&k_empty[st]);
-        if (j > 0) ok = issue_pv(j - 1);
+        tc_commit(&s_full[t]);
+      };
+      // O_t += P_t V_j; P_t sits (bf16, two per column) over S_t in TMEM and
+      // V_j is [key][d]: MN-major for this product (d contiguous); 16 keys =
+      // two 8-row groups of 1024 bytes, d slabs 128*128 bytes apart.
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!mbar_wait(&p_ready[t], j & 1, ctl, kSitePReady)) return false;
+        tc_fence_after();
+        const uint32_t vbase = aV + (j % S) * L::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(vbase + kk * 2048, kBN * 128, 1024), kIdescO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&pv_done[t]);
+        return true;
+      };
+
+      bool ok = mbar_wait(q_full, 0, ctl, kSiteQFull) && mbar_wait(&k_full[0], 0, ctl, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(&k_empty[0]);
       }
-      if (ok) issue_pv(n_kv - 1);
+      for (int j = 1; ok && j < n_kv; ++j) {
+        const int pj = j - 1;
+        if (!(ok = mbar_wait(&v_full[pj % S], (pj / S) & 1, ctl, kSiteVFull))) break;
+        tc_fence_after();
+        if (pj < n0 && !(ok = issue_pv(0, pj))) break;
+        if (!(ok = mbar_wait(&k_full[j % S], (j / S) & 1, ctl, kSiteKFull))) break;
+        tc_fence_after();
+        if (j < n0) issue_s(0, j);
+        if (!(ok = issue_pv(1, pj))) break;
+        tc_commit(&v_empty[pj % S]);
+        issue_s(1, j);
+        tc_commit(&k_empty[j % S]);
+      }
+      if (ok) {
+        const int pj = n_kv - 1;
+        ok = mbar_wait(&v_full[pj % S], (pj / S) & 1, ctl, kSiteVFull);
+        if (ok) {
+          tc_fence_after();
+          if (pj < n0) ok = issue_pv(0, pj);
+          if (ok) ok = issue_pv(1, pj);
+          tc_commit(&v_empty[pj % S]);
+        }
+      }
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
-  } else if (warp >= 4) {
+  } else {
+    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const float c = p.scale_log2;
-    const bool neg = p.neg != 0;
-    float m_run = -INFINITY, l_run = 0.0f;
-    bool ok = true;
-
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      ok = mbar_wait(&s_full[b], (j >> 1) & 1, ctl, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tS = tS0 + b * 128 + lane_base;
-      uint32_t s[4][32];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, s[q4]);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(s[q4]);
-
-      // Masking: causal diagonal block and the ragged last key block.
-      const bool need_mask = (CAUSAL && j == qblk) || ((j + 1) * kBN > N);
-      int lim = kBN - 1;  // last visible column of this row
-      if (need_mask) {
-        lim = min(lim, N - 1 - j * kBN);
-        if (CAUSAL && j == qblk) lim = min(lim, row);
-        const uint32_t hide = __float_as_uint(neg ? INFINITY : -INFINITY);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (q4 * 32 + i > lim) s[q4][i] = hide;
-      }
-
-      // Block max of t = s * c (a min of s when the scale is negative).
-      float mx;
-      if (!neg) {
-        float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            m0 = fmaxf(m0, __uint_as_float(s[q4][i]));
-            m1 = fmaxf(m1, __uint_as_float(s[q4][i + 1]));
-          }
-        mx = fmaxf(m0, m1);
-      } else {
-        float m0 = INFINITY, m1 = INFINITY;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            m0 = fminf(m0, __uint_as_float(s[q4][i]));
-            m1 = fminf(m1, __uint_as_float(s[q4][i + 1]));
-          }
-        mx = fminf(m0, m1);
-      }
-      const float m_cand = mx * c;
-      const bool grow = m_cand > m_run + kRescaleThreshold;
-      float alpha = 1.0f;
-      if (grow) {
-        alpha = ex2(m_run - m_cand);
-        m_run = m_cand;
-      }
-      l_run *= alpha;
-      const float neg_m = -m_run;
-
-      // P = exp2(t - m) as bf16 pairs over the first 64 columns of S_j.
-      float sum0 = 0.0f, sum1 = 0.0f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int q4 = 2 * h + q2;
-            float p0 = ex2(fmaf(__uint_as_float(s[q4][i]), c, neg_m));
-            float p1 = ex2(fmaf(__uint_as_float(s[q4][i + 1]), c, neg_m));
-            if (need_mask) {
-              p0 = (q4 * 32 + i <= lim) ? p0 : 0.0f;
-              p1 = (q4 * 32 + i + 1 <= lim) ? p1 : 0.0f;
-            }
-            sum0 += p0;
-            sum1 += p1;
-            pk[q2 * 16 + i / 2] = pack_bf16x2(p0, p1);
-          }
-        tmem_st32(tS + h * 32, pk);
-      }
-      l_run += sum0 + sum1;
-      tmem_st_wait();
-
-      // O of the previous block must be complete before it is rescaled and
-      // before the next product accumulates into it.
-      if (j > 0) {
-        ok = mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl, kSitePvDone);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        if (__any_sync(0xffffffffu, grow)) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_base + ch * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + lane_base + ch * 32, o);
-          }
-          tmem_st_wait();
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&p_ready[b]);
-    }
-
-    // Epilogue: O / l in bf16 and the natural-log logsumexp.
-    if (ok) {
-      const int last = n_kv - 1;
-      ok = mbar_wait(&pv_done[last & 1], (last >> 1) & 1, ctl, kSitePvDone);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l_run;
-      const int grow_row = qblk * kBM + row;
-      const bool store = grow_row < N;
-      __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + grow_row) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_base + ch * 32, o);
-        tmem_ld_wait(o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (store) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-      }
-      if (store) p.lse[static_cast<size_t>(bh) * N + grow_row] = (m_run + log2f(l_run)) * kLn2;
-    }
+    const int t = warp >> 2;
+    SoftmaxArgs a;
+    a.s_full = &s_full[t];
+    a.p_ready = &p_ready[t];
+    a.pv_done = &pv_done[t];
+    a.tS = tmem + t * 128;
+    a.tO = tmem + 256 + t * D;
+    a.n_kv = t ? n1 : n0;
+    a.diag = CAUSAL ? 2 * qb + t : -1;
+    a.grow0 = qb * 2 * kBM + t * kBM;
+    softmax_tile<D>(a, p, ctl, bh, warp, lane);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -384,7 +446,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_qblk);
-  kern<<<grid, 256, L::kSmemRequest, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, L::kSmemRequest, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

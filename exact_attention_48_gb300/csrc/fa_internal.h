@@ -34,7 +34,7 @@ struct FwdParams {
   int *status;        // device status block (2 ints)
   int N;
   int BH;
-  int num_qblk;       // ceil(N / 128)
+  int num_qblk;       // ceil(N / 256): one CTA per 256 query rows
   float scale_log2;   // scale * log2(e)
   int neg;            // scale < 0
 };
