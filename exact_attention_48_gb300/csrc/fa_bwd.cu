@@ -23,10 +23,12 @@
 //   warp 0      TMA producer: K_j, V_j once; Q_i and dO_i into a 2-stage ring
 //   warp 1      MMA issuer (one thread)
 //   warp 2      owns the TMEM allocation
-//   warps 4..7  one key row per thread: P^T, dS^T from S^T, dP^T, LSE, D;
-//               P^T goes to TMEM (A operand of dV += P^T dO), dS^T to shared
-//               memory (operand of dK += dS^T Q and, read MN-major, of
-//               dQ = dS K); final dV epilogue
+//   warps 4..7  one key row per thread, in two phases per query block:
+//               P^T from S^T and the saved LSE, written as bf16 to TMEM (A
+//               operand of dV += P^T dO) and kept in registers; then
+//               dS^T = P^T o (dP^T - D) written as bf16 to shared memory
+//               (operand of dK += dS^T Q and, read MN-major, of dQ = dS K);
+//               final dV epilogue
 //   warps 8..11 one query row per thread: drain dQ_i from TMEM into the
 //               fp32 accumulator; final dK epilogue
 //
@@ -120,8 +122,9 @@ struct BwdLayout {
   static constexpr uint32_t kOffDO = kOffQ + kStages * kTile;      // kStages tiles
   static constexpr uint32_t kOffDS = kOffDO + kStages * kTile;     // [128 keys][128 queries] bf16
   static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
-  // kv_full, qdo_full[2], qdo_empty[2], sdp_full, pds_ready, dq_full, dq_empty, acc_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 6;
+  // kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty,
+  // acc_done, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 8;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemRequest = kBytes + 1024;
@@ -133,6 +136,13 @@ struct BwdLayout {
 };
 
 constexpr uint32_t kTmemCols = 512;
+
+// Register split over the three warpgroups: 168 per thread at launch
+// (384 x 168 fits the SM); control 120, key-row warps 240, dQ drain 144:
+// 128 * (120 + 240 + 144) = 384 * 168, and per SM sub-partition (one warp of
+// each warpgroup) 32 * (120 + 240 + 144) <= 16384.
+constexpr uint32_t kRegsLaunch = 168, kRegsControl = 120, kRegsRows = 240, kRegsDrain = 144;
+static_assert(128 * (kRegsControl + kRegsRows + kRegsDrain) <= 384 * kRegsLaunch, "register split");
 
 // Byte offset of element (row, col) in a 128-byte-swizzled tile made of
 // 64-column slabs of `rows` rows (the layout the TMA loads produce).
@@ -155,9 +165,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t *kv_full = bars;
   uint64_t *qdo_full = bars + 1;
   uint64_t *qdo_empty = qdo_full + S;
-  uint64_t *sdp_full = qdo_empty + S;
-  uint64_t *pds_ready = sdp_full + 1;
-  uint64_t *dq_full = pds_ready + 1;
+  uint64_t *s_full = qdo_empty + S;
+  uint64_t *dp_full = s_full + 1;
+  uint64_t *p_ready = dp_full + 1;
+  uint64_t *ds_ready = p_ready + 1;
+  uint64_t *dq_full = ds_ready + 1;
   uint64_t *dq_empty = dq_full + 1;
   uint64_t *acc_done = dq_empty + 1;
   uint64_t *drain = acc_done + 1;
@@ -191,8 +203,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(pds_ready, 128);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(ds_ready, 128);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
@@ -215,9 +229,10 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t *sDO = smem + L::kOffDO;
   uint8_t *sDS = smem + L::kOffDS;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    regs_decrease<kRegsControl>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -245,10 +260,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_drain(kv_full, 0);
         for (int t = (issued > S ? issued - S : 0); t < issued; ++t) mbar_drain(&qdo_full[t % S], (t / S) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescSq = idesc_bf16(kBlk, kBlk, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKB = idesc_bf16(kBlk, D, false, true);      // dV (TMEM A), dK
       constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, true, true);        // dQ
@@ -256,61 +269,80 @@ __global__ void __launch_bounds__(384, 1)
                      aDS = smem_addr(sDS);
       const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
                      tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
-      bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull);
-      tc_fence_after();
-      for (int t = 0; ok && t < n_q; ++t) {
-        const int st = t % S;
-        if (!(ok = mbar_wait(&qdo_full[st], (t / S) & 1, ctl, kSiteDoFull))) break;
-        tc_fence_after();
-        const uint32_t q_base = aQ + st * L::kTile, do_base = aDO + st * L::kTile;
-        // S^T = K Q_i^T   (both K-major over d)
-#pragma unroll
+      // S^T = K Q_t^T and dP^T = V dO_t^T (all operands K-major over d)
+      auto issue_s = [&](int t) {
+        const uint32_t q_base = aQ + (t % S) * L::kTile;
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
           mma_ss(tS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), kIdescSq, kk > 0);
         }
-        if (L::kDqAliasesDP && t > 0) {
-          // dQ_{t-1} sits in the dP^T columns until it has been drained
-          if (!(ok = mbar_wait(dq_empty, (t - 1) & 1, ctl, kSiteDqEmpty))) break;
-          tc_fence_after();
-        }
-        // dP^T = V dO_i^T
-#pragma unroll
+        tc_commit(s_full);
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t do_base = aDO + (t % S) * L::kTile;
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
           mma_ss(tDP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024), kIdescSq, kk > 0);
         }
-        tc_commit(sdp_full);
-        if (!(ok = mbar_wait(pds_ready, t & 1, ctl, kSiteDsReady))) break;
+        tc_commit(dp_full);
+      };
+
+      // Order per query block t:  dV_t, dQ_t, dK_t, S^T_{t+1}, dP^T_{t+1}.
+      // The row warps form P_{t+1} while dP^T_{t+1} runs and dS_{t+1} while
+      // dV_{t+1} runs; dQ_t drains while dK_t and S^T_{t+1} run.
+      bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull) && mbar_wait(&qdo_full[0], 0, ctl, kSiteDoFull);
+      if (ok) {
         tc_fence_after();
-        // dV += P^T dO_i   (P^T from TMEM; dO_i is MN-major over d)
-#pragma unroll
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; ok && t < n_q; ++t) {
+        const int st = t % S;
+        const uint32_t q_base = aQ + st * L::kTile, do_base = aDO + st * L::kTile;
+        // dV += P^T dO_t   (P^T from TMEM; dO_t is MN-major over d)
+        if (!(ok = mbar_wait(p_ready, t & 1, ctl, kSitePReady))) break;
+        tc_fence_after();
+#pragma unroll 1
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_base + kk * 2048, kBlk * 128, 1024), kIdescKB, (t > 0 || kk > 0));
-        // dK += dS^T Q_i   (dS^T K-major over queries; Q_i MN-major over d)
-#pragma unroll
+        if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
+        if (!L::kDqAliasesDP && t > 0 && !(ok = mbar_wait(dq_empty, (t - 1) & 1, ctl, kSiteDqEmpty))) break;
+        tc_fence_after();
+        // dQ_t = dS K   (dS read MN-major from the dS^T tile; K MN-major over d)
+#pragma unroll 1
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ss(tDQ, sdesc_sw128(aDS + kk * 2048, kBlk * 128, 1024), sdesc_sw128(aK + kk * 2048, kBlk * 128, 1024),
+                 kIdescQ, kk > 0);
+        tc_commit(dq_full);
+        // dK += dS^T Q_t   (dS^T K-major over queries; Q_t MN-major over d)
+#pragma unroll 1
         for (int kk = 0; kk < kBlk / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
           mma_ss(tDK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(q_base + kk * 2048, kBlk * 128, 1024), kIdescKB,
                  (t > 0 || kk > 0));
         }
-        if (!L::kDqAliasesDP && t > 0) {
-          if (!(ok = mbar_wait(dq_empty, (t - 1) & 1, ctl, kSiteDqEmpty))) break;
-          tc_fence_after();
-        }
-        // dQ_i = dS K   (dS read MN-major from the dS^T tile; K MN-major over d)
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tDQ, sdesc_sw128(aDS + kk * 2048, kBlk * 128, 1024), sdesc_sw128(aK + kk * 2048, kBlk * 128, 1024),
-                 kIdescQ, kk > 0);
-        tc_commit(dq_full);
         tc_commit(&qdo_empty[st]);
+        if (t + 1 < n_q) {
+          const int nst = (t + 1) % S;
+          if (!(ok = mbar_wait(&qdo_full[nst], ((t + 1) / S) & 1, ctl, kSiteDoFull))) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          if (L::kDqAliasesDP) {
+            // dQ_t sits in the dP^T columns until it has been drained
+            if (!(ok = mbar_wait(dq_empty, t & 1, ctl, kSiteDqEmpty))) break;
+            tc_fence_after();
+          }
+          issue_dp(t + 1);
+        }
       }
       if (ok) tc_commit(acc_done);
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp < 8) {
+    regs_increase<kRegsRows>();
     // ------------------------------------------------------------ P^T, dS^T (one key row per thread)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the block
@@ -329,45 +361,78 @@ __global__ void __launch_bounds__(384, 1)
       // per-query statistics of this block (same for every thread: L1 broadcasts)
       const float4 *lse4 = reinterpret_cast<const float4 *>(lse2_h + i * kBlk);
       const float4 *del4 = reinterpret_cast<const float4 *>(delta_h + i * kBlk);
-      ok = mbar_wait(sdp_full, t & 1, ctl, kSiteSFull);
+      const bool diag = CAUSAL && (i == jblk);
+      const bool key_ok = key < N;
+
+      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [0, 64).
+      ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = CAUSAL && (i == jblk);
-      const bool key_ok = key < N;
-#pragma unroll 1
+      uint32_t pk[64];  // P^T row, bf16 pairs, kept for phase 2
+#pragma unroll
       for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t sv[32], dpv[32];
+        uint32_t sv[32];
         tmem_ld32(tS + ch * 32, sv);
-        tmem_ld32(tDP + ch * 32, dpv);
         tmem_ld_wait(sv);
-        tmem_ld_wait(dpv);
-        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int qc = ch * 32 + e;  // query column within the block
           const float4 l4 = __ldg(lse4 + qc / 4);
-          const float4 d4 = __ldg(del4 + qc / 4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], dsr[4];
+          const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), make_float2(c, c),
+                                   make_float2(-l4.x, -l4.y));
+          const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                   make_float2(c, c), make_float2(-l4.z, -l4.w));
+          float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            float pv = ex2(fmaf(__uint_as_float(sv[e + u]), c, -lv[u]));
-            if (diag) pv = (qc + u >= r) ? pv : 0.0f;  // key r visible to query qc+u iff r <= qc+u
-            if (!key_ok) pv = 0.0f;
-            pr[u] = pv;
-            dsr[u] = pv * (__uint_as_float(dpv[e + u]) - dv[u]);
+            if (diag) pr[u] = (qc + u >= r) ? pr[u] : 0.0f;  // key r visible to query qc+u iff r <= qc+u
+            if (!key_ok) pr[u] = 0.0f;
           }
-          pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
-          pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
-          dk[e / 2] = pack_bf16x2(dsr[0], dsr[1]);
-          dk[e / 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
+          pk[qc / 2] = pack_bf16x2(pr[0], pr[1]);
+          pk[qc / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
         }
-        // P^T: bf16 pairs over columns [16 ch, 16 ch + 16) of S^T (already read)
-        tmem_st16(tS + ch * 16, pk);
+        // columns [16 ch, 16 ch + 16) of S^T hold queries already read
+        uint32_t part[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) part[u] = pk[ch * 16 + u];
+        tmem_st16(tS + ch * 16, part);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 into the swizzled dS^T tile.
+      ok = mbar_wait(dp_full, t & 1, ctl, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) {
+        uint32_t dpv[32];
+        tmem_ld32(tDP + ch * 32, dpv);
+        tmem_ld_wait(dpv);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int qc = ch * 32 + e;
+          const float4 d4 = __ldg(del4 + qc / 4);
+          const uint32_t p01 = pk[qc / 2], p23 = pk[qc / 2 + 1];
+          const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                   make_float2(-d4.x, -d4.y));
+          const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                   make_float2(-d4.z, -d4.w));
+          const float2 ds01 = ffma2(make_float2(__uint_as_float(p01 << 16), __uint_as_float(p01 & 0xFFFF0000u)), g01,
+                                    make_float2(0.f, 0.f));
+          const float2 ds23 = ffma2(make_float2(__uint_as_float(p23 << 16), __uint_as_float(p23 & 0xFFFF0000u)), g23,
+                                    make_float2(0.f, 0.f));
+          dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
+          dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
+        }
         // dS^T row r, queries [32 ch, 32 ch + 32): four 16-byte chunks
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -377,10 +442,9 @@ __global__ void __launch_bounds__(384, 1)
                        : "memory");
         }
       }
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(pds_ready);
+      mbar_arrive(ds_ready);
     }
     // dV epilogue
     if (ok) {
@@ -406,7 +470,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else {
+    regs_decrease<kRegsDrain>();
     // ------------------------------------------------------------ dQ drain (one query row per thread)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;

@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_t = Q_t K_j^T (both operands K-major over d)
       auto issue_s = [&](int t, int j) {
         const uint32_t kbase = aK + (j % S) * L::kKVBytes, qbase = aQ + t * L::kQTile;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           mma_ss(tmem + t * 128, sdesc_sw128(qbase + koff, 16, 1024), sdesc_sw128(kbase + koff, 16, 1024), kIdescS,
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&p_ready[t], j & 1, ctl, kSitePReady)) return false;
         tc_fence_after();
         const uint32_t vbase = aV + (j % S) * L::kKVBytes;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(vbase + kk * 2048, kBN * 128, 1024), kIdescO,
                  (j > 0 || kk > 0) ? 1u : 0u);
