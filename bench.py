@@ -258,7 +258,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from exact_attention_48_gb300 import fa_bwd, fa_bwd_workspace_bytes, fa_device_status, fa_fwd
-    from exact_attention_48_gb300.binding import fa_debug_time_next_bwd_main
+    from exact_attention_48_gb300.binding import fa_debug_time_next_bwd
     from exact_attention_48_gb300.inputs import draw
 
     w = workload(args)
@@ -276,10 +276,10 @@ def run_ours(args):
         fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
         if evs is not None:
             evs[1].record(stream)
-            fa_debug_time_next_bwd_main(evs[2], evs[3])
+            fa_debug_time_next_bwd(evs[2], evs[3], evs[4])
         fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         if evs is not None:
-            evs[4].record(stream)
+            evs[5].record(stream)
 
     for _ in range(max(args.warmup, 3 if args.warmup >= 3 else args.warmup)):
         step()
@@ -295,7 +295,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.6)  # let the sampler start
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -314,17 +314,23 @@ def run_ours(args):
     flops_step = w.flops_fwd() + w.flops_bwd()
     value, elapsed_ms = aggregate_throughput(flops_step, args.steps, start.elapsed_time(stop), world, "cuda")
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
-    bwd_main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
     fwd_tf = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
     bwd_tf = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12
-    bwd_main_tf = w.flops_bwd() / (bwd_main_ms * 1e-3) / 1e12
-    # dominant kernel: the backward main kernel (the forward kernel is timed beside it)
-    dom, dom_ms, dom_tf = ("fa_bwd_main_kernel", bwd_main_ms, bwd_main_tf) if bwd_main_ms >= fwd_ms else \
-        ("fa_fwd_kernel", fwd_ms, fwd_tf)
+    # Per-kernel tensor work actually executed (the dense products of each
+    # kernel, in units of the forward's 4*B*H*N^2*d): forward 1.0, dK/dV 2.0
+    # (S^T, dP^T, dV, dK), dQ 1.5 (S, dP, dQ).  The backward headline keeps
+    # the 2.5x count of the metric and credits no recomputation.
+    kernels = [("fa_fwd_kernel", fwd_ms, 1.0 * w.flops_fwd()),
+               ("fa_bwd_dkdv_kernel", dkdv_ms, 2.0 * w.flops_fwd()),
+               ("fa_bwd_dq_kernel", dq_ms, 1.5 * w.flops_fwd())]
+    dom, dom_ms, dom_flops = max(kernels, key=lambda k: k[1])
+    dom_tf = dom_flops / (dom_ms * 1e-3) / 1e12
     traffic = traffic_record(dom)
 
     line = {
@@ -335,12 +341,14 @@ def run_ours(args):
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_sustained": fwd_tf / peak_sus,
                 "frac_of_burst": fwd_tf / peak_burst},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_sustained": bwd_tf / peak_sus,
-                "frac_of_burst": bwd_tf / peak_burst, "main_kernel_ms": bwd_main_ms},
+                "frac_of_burst": bwd_tf / peak_burst},
+        "kernels": {name: {"ms": ms, "tensor_tflops_executed": fl / (ms * 1e-3) / 1e12,
+                           "frac_of_sustained": fl / (ms * 1e-3) / 1e12 / peak_sus} for name, ms, fl in kernels},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": dom_tf,
                      "peak": peak_sus, "unit": "TFLOP/s", "frac": dom_tf / peak_sus,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
-                     "traffic": traffic},
-        "gpu_launches": 4 * args.steps,
+                     "flops_per_launch": dom_flops, "traffic": traffic},
+        "gpu_launches": 4 * args.steps,  # fwd; bwd pre, dK/dV, dQ
         "clocks": clk,
     }
 

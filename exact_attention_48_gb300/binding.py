@@ -59,8 +59,8 @@ def library(path: str | None = None):
             lib.fa_device_status.restype = i
             lib.fa_debug_last_wait_site.argtypes = []
             lib.fa_debug_last_wait_site.restype = i
-            lib.fa_debug_time_next_bwd_main.argtypes = [vp, vp]
-            lib.fa_debug_time_next_bwd_main.restype = i
+            lib.fa_debug_time_next_bwd.argtypes = [vp, vp, vp]
+            lib.fa_debug_time_next_bwd.restype = i
             lib.fa_status_string.argtypes = [i]
             lib.fa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -154,13 +154,14 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
-def fa_debug_time_next_bwd_main(start: "torch.cuda.Event", stop: "torch.cuda.Event") -> None:
-    """Have the next fa_bwd of this thread record the two events around its main kernel."""
-    start.record()  # make sure torch has created the underlying CUDA events
-    stop.record()
-    rc = library().fa_debug_time_next_bwd_main(start.cuda_event, stop.cuda_event)
+def fa_debug_time_next_bwd(start, mid, stop) -> None:
+    """Have the next fa_bwd of this thread record three torch.cuda.Events:
+    before its dK/dV kernel, between it and its dQ kernel, after the dQ kernel."""
+    for e in (start, mid, stop):
+        e.record()  # make sure torch has created the underlying CUDA events
+    rc = library().fa_debug_time_next_bwd(start.cuda_event, mid.cuda_event, stop.cuda_event)
     if rc != FA_OK:
-        raise FaError(rc, "fa_debug_time_next_bwd_main")
+        raise FaError(rc, "fa_debug_time_next_bwd")
 
 
 def fa_device_status(stream=None) -> int:

@@ -67,8 +67,8 @@ fa_status_t check_common(int B, int H, int N, int d, int causal, float scale) {
   return FA_OK;
 }
 
-// Events the next fa_bwd call of this thread records around its main kernel.
-thread_local cudaEvent_t t_bwd_ev_start = nullptr, t_bwd_ev_stop = nullptr;
+// Events the next fa_bwd call of this thread records around its kernels.
+thread_local cudaEvent_t t_bwd_ev[3] = {nullptr, nullptr, nullptr};
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -127,9 +127,8 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_common(B, H, N, d, 0, 1.0f) != FA_OK) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t padded_rows = static_cast<size_t>(B) * H * ((N + 127) / 128) * 128;
-  return round256(rows * d * 4) + 2 * round256(padded_rows * 4);
+  return 2 * round256(padded_rows * 4);
 }
 
 fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dO, const float *lse,
@@ -170,15 +169,13 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return FA_ERR_CUDA;
     owned = true;
   }
-  const size_t rows = static_cast<size_t>(BH) * N;
   BwdParams p{};
   p.o = static_cast<const __nv_bfloat16 *>(o);
   p.dout = static_cast<const __nv_bfloat16 *>(dO);
   p.lse = lse;
-  p.dq_acc = static_cast<float *>(ws);
   const size_t padded_rows = static_cast<size_t>(BH) * ((N + 127) / 128) * 128;
-  p.delta = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round256(rows * d * 4));
-  p.lse2 = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round256(rows * d * 4) + round256(padded_rows * 4));
+  p.delta = static_cast<float *>(ws);
+  p.lse2 = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round256(padded_rows * 4));
   p.dq = static_cast<__nv_bfloat16 *>(dq);
   p.dk = static_cast<__nv_bfloat16 *>(dk);
   p.dv = static_cast<__nv_bfloat16 *>(dv);
@@ -189,9 +186,10 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status_t rc = FA_OK;
-  cudaEvent_t ev0 = t_bwd_ev_start, ev1 = t_bwd_ev_stop;
-  t_bwd_ev_start = t_bwd_ev_stop = nullptr;
-  if (!p.status || launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream, ev0, ev1) != cudaSuccess) rc = FA_ERR_CUDA;
+  const cudaEvent_t ev[3] = {t_bwd_ev[0], t_bwd_ev[1], t_bwd_ev[2]};
+  t_bwd_ev[0] = t_bwd_ev[1] = t_bwd_ev[2] = nullptr;
+  if (!p.status || launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream, ev[0] ? ev : nullptr) != cudaSuccess)
+    rc = FA_ERR_CUDA;
   if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   return rc;
 }
@@ -208,10 +206,11 @@ fa_status_t fa_device_status(cudaStream_t stream) {
   return FA_OK;
 }
 
-fa_status_t fa_debug_time_next_bwd_main(cudaEvent_t start, cudaEvent_t stop) {
-  if (!start || !stop) return FA_ERR_INVALID_ARGUMENT;
-  t_bwd_ev_start = start;
-  t_bwd_ev_stop = stop;
+fa_status_t fa_debug_time_next_bwd(cudaEvent_t start, cudaEvent_t mid, cudaEvent_t stop) {
+  if (!start || !mid || !stop) return FA_ERR_INVALID_ARGUMENT;
+  t_bwd_ev[0] = start;
+  t_bwd_ev[1] = mid;
+  t_bwd_ev[2] = stop;
   return FA_OK;
 }
 

@@ -8,37 +8,25 @@
 //     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D = rowsum(dO o O),
 //     dK = s dS^T Q,  dQ = s dS K.
 //
-// Three launches on the caller's stream:
-//   1. fa_bwd_pre_kernel   D = rowsum(dO o O) per query row (fp32), the
+// Three launches on the caller's stream, none with atomics, so every
+// output is bitwise reproducible:
+//   1. fa_bwd_pre_kernel   D = rowsum(dO o O) per query row (fp32) and the
 //                          saved logsumexp in log2 units, both padded to
-//                          whole blocks, and a zeroed fp32 dQ accumulator.
-//   2. fa_bwd_main_kernel  one CTA per (head, block of 128 keys): K_j and V_j
+//                          whole blocks of 128 rows.
+//   2. fa_bwd_dkdv_kernel  one CTA per (head, block of 128 keys): K_j, V_j
 //                          stay in shared memory, dK_j and dV_j accumulate in
-//                          TMEM over all query blocks i, and each block's
-//                          dQ_i contribution is added into the fp32
-//                          accumulator with vector atomics.
-//   3. fa_bwd_dq_kernel    dq = bf16(s * accumulator).
+//                          TMEM over the query blocks (4 products per block).
+//   3. fa_bwd_dq_kernel    one CTA per (head, block of 128 queries): Q_i, dO_i
+//                          stay in shared memory, dQ_i accumulates in TMEM
+//                          over the key blocks (3 products per block).
+// Splitting dQ off costs two recomputed products per block pair but removes
+// the fp32 reduction of dQ across key blocks through L2, which otherwise
+// bounds the backward pass.
 //
-// Main kernel roles (384 threads):
-//   warp 0      TMA producer: K_j, V_j once; Q_i and dO_i into a 2-stage ring
-//   warp 1      MMA issuer (one thread)
-//   warp 2      owns the TMEM allocation
-//   warps 4..7  one key row per thread, in two phases per query block:
-//               P^T from S^T and the saved LSE, written as bf16 to TMEM (A
-//               operand of dV += P^T dO) and kept in registers; then
-//               dS^T = P^T o (dP^T - D) written as bf16 to shared memory
-//               (operand of dK += dS^T Q and, read MN-major, of dQ = dS K);
-//               final dV epilogue
-//   warps 8..11 one query row per thread: drain dQ_i from TMEM into the
-//               fp32 accumulator; final dK epilogue
-//
-// The products are computed transposed (S^T = K Q_i^T, dP^T = V dO_i^T) so
-// that the key row, which owns dK/dV, is the TMEM lane.
-//
-// TMEM columns: S^T [0,128) (P^T as bf16 pairs over its first 64 columns),
-// dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).  For d = 128 that is
-// all 512 columns and dQ_i reuses the dP^T columns once dS has been formed;
-// for d = 64 dQ has its own columns [384,448).
+// Both main kernels: warp 0 TMA producer, warp 1 MMA issuer (one thread),
+// warp 2 TMEM owner, warps 4..7 one row per thread (key row in dK/dV, query
+// row in dQ), working in two phases per block: P from the scores, then dS
+// from dP.
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -47,17 +35,19 @@ namespace fa {
 
 namespace {
 
-constexpr int kBlk = 128;  // keys per CTA and queries per step
+constexpr int kBlk = 128;  // rows per block, keys and queries alike
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 256;
 
 // ------------------------------------------------------------------ pre
 
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   // One padded row per kTpr threads: rows q < N of every head get
-  // D = rowsum(dO o O), lse * log2(e) and a zeroed dQ accumulator row; the
-  // padding rows up to the next multiple of 128 get D = 0 and lse = +inf
-  // (probability 0), so the main kernel reads whole blocks without checks.
+  // D = rowsum(dO o O) and lse * log2(e); the padding rows up to the next
+  // multiple of 128 get D = 0 and lse = +inf (probability 0), so the main
+  // kernels read whole blocks without checks.
   constexpr int kTpr = D / 8;  // threads per row: 8 bf16 (16 bytes) each
   constexpr int kRowsPerBlock = 256 / kTpr;
   const int Np = p.num_blk * kBlk;
@@ -81,9 +71,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
       acc = fmaf(a.x, b.x, acc);
       acc = fmaf(a.y, b.y, acc);
     }
-    float4 *z = reinterpret_cast<float4 *>(p.dq_acc + row * D) + 2 * part;
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -93,56 +80,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   }
 }
 
-// ------------------------------------------------------------------ dq convert
-
-template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
-  const long long n4 = static_cast<long long>(p.BH) * p.N * D / 4;
-  const float s = p.scale;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4 *>(p.dq_acc)[i];
-    uint2 out;
-    out.x = pack_bf16x2(a.x * s, a.y * s);
-    out.y = pack_bf16x2(a.z * s, a.w * s);
-    reinterpret_cast<uint2 *>(p.dq)[i] = out;
-  }
-}
-
-// ------------------------------------------------------------------ main
-
-template <int D>
-struct BwdLayout {
-  static constexpr int kSlabs = D / 64;
-  static constexpr int kStages = 2;
-  static constexpr uint32_t kTile = kBlk * D * 2;  // one [128][D] bf16 tile
-  static constexpr uint32_t kOffK = 0;
-  static constexpr uint32_t kOffV = kOffK + kTile;
-  static constexpr uint32_t kOffQ = kOffV + kTile;                 // kStages tiles
-  static constexpr uint32_t kOffDO = kOffQ + kStages * kTile;      // kStages tiles
-  static constexpr uint32_t kOffDS = kOffDO + kStages * kTile;     // [128 keys][128 queries] bf16
-  static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
-  // kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty,
-  // acc_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 8;
-  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kBytes = kOffMisc + 16;
-  static constexpr uint32_t kSmemRequest = kBytes + 1024;
-  static_assert(kSmemRequest <= 232448, "shared memory budget");
-  // TMEM columns
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static constexpr bool kDqAliasesDP = (D == 128);
-  static constexpr uint32_t kColDQ = kDqAliasesDP ? kColDP : 384;
-};
-
-constexpr uint32_t kTmemCols = 512;
-
-// Register split over the three warpgroups: 168 per thread at launch
-// (384 x 168 fits the SM); control 120, key-row warps 240, dQ drain 144:
-// 128 * (120 + 240 + 144) = 384 * 168, and per SM sub-partition (one warp of
-// each warpgroup) 32 * (120 + 240 + 144) <= 16384.
-constexpr uint32_t kRegsLaunch = 168, kRegsControl = 120, kRegsRows = 240, kRegsDrain = 144;
-static_assert(128 * (kRegsControl + kRegsRows + kRegsDrain) <= 384 * kRegsLaunch, "register split");
+// ------------------------------------------------------------------ shared pieces
 
 // Byte offset of element (row, col) in a 128-byte-swizzled tile made of
 // 64-column slabs of `rows` rows (the layout the TMA loads produce).
@@ -151,27 +89,89 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
                                (col & 7) * 2);
 }
 
+// 32 bf16 values (16 pairs) of row r of a [128 x 128] bf16 tile, starting at
+// column col0, into shared memory with the 128-byte swizzle, 16 bytes at a
+// time.
+__device__ __forceinline__ void store_row_sw128(uint32_t tile, int r, int col0, const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t addr = tile + sw128_offset(r, col0 + u * 8, kBlk);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * u]), "r"(v[4 * u + 1]),
+                 "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+                 : "memory");
+  }
+}
+
+// One row of a TMEM accumulator (lane = row, D fp32 columns), times `mul`,
+// into a bf16 row of global memory.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16 *dst, bool store, float mul) {
+#pragma unroll 1
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(taddr + ch * 32, v);
+    tmem_ld_wait(v);
+    if (store) {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        d4[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+    }
+  }
+}
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kStages = 2;
+  static constexpr uint32_t kTile = kBlk * D * 2;  // one [128][D] bf16 tile
+  // Both kernels hold two resident tiles (K, V or Q, dO), a 2-stage ring of
+  // two tiles (Q, dO or K, V) and one [128][128] bf16 dS tile.
+  static constexpr uint32_t kOffRes0 = 0;
+  static constexpr uint32_t kOffRes1 = kOffRes0 + kTile;
+  static constexpr uint32_t kOffRing0 = kOffRes1 + kTile;             // kStages tiles
+  static constexpr uint32_t kOffRing1 = kOffRing0 + kStages * kTile;  // kStages tiles
+  static constexpr uint32_t kOffDS = kOffRing1 + kStages * kTile;
+  static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
+  static constexpr int kNumBars = 16;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kOffMisc + 16;
+  static constexpr uint32_t kSmemRequest = kBytes + 1024;
+  static_assert(kSmemRequest <= 232448, "shared memory budget");
+};
+
+// ------------------------------------------------------------------ dK, dV
+
+// TMEM columns: S^T [0,128) (P^T as bf16 pairs over its first 64 columns),
+// dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The products are
+// formed transposed (S^T = K Q^T, dP^T = V dO^T) so the key row, which owns
+// dK and dV, is the TMEM lane.  MMA order per query block t:
+//   dV(t), S^T(t+1), dK(t), dP^T(t+1)
+// so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
+// dV(t+1) and S^T(t+2) run.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
-    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
   using L = BwdLayout<D>;
   constexpr int S = L::kStages;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
   uint64_t *kv_full = bars;
-  uint64_t *qdo_full = bars + 1;
-  uint64_t *qdo_empty = qdo_full + S;
+  uint64_t *qdo_full = bars + 1;       // [S]
+  uint64_t *qdo_empty = qdo_full + S;  // [S]
   uint64_t *s_full = qdo_empty + S;
   uint64_t *dp_full = s_full + 1;
   uint64_t *p_ready = dp_full + 1;
   uint64_t *ds_ready = p_ready + 1;
-  uint64_t *dq_full = ds_ready + 1;
-  uint64_t *dq_empty = dq_full + 1;
-  uint64_t *acc_done = dq_empty + 1;
+  uint64_t *acc_done = ds_ready + 1;
   uint64_t *drain = acc_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
@@ -192,10 +192,9 @@ __global__ void __launch_bounds__(384, 1)
     bh = static_cast<int>(blockIdx.x) / nblk;
     jblk = static_cast<int>(blockIdx.x) % nblk;
   }
-  // Query blocks visited: causal i = j .. nblk-1; otherwise all blocks,
-  // starting at j so that the CTAs of one head add into different dQ rows.
+  // Query blocks visited: causal i = j .. nblk-1; otherwise all of them.
   const int n_q = CAUSAL ? (nblk - jblk) : nblk;
-  auto qblock = [&](int t) { return CAUSAL ? jblk + t : (jblk + t) % nblk; };
+  const int i0 = CAUSAL ? jblk : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -207,8 +206,6 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 128);
     mbar_init(ds_ready, 128);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -223,16 +220,15 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t *sK = smem + L::kOffK;
-  uint8_t *sV = smem + L::kOffV;
-  uint8_t *sQ = smem + L::kOffQ;
-  uint8_t *sDO = smem + L::kOffDO;
+  uint8_t *sK = smem + L::kOffRes0;
+  uint8_t *sV = smem + L::kOffRes1;
+  uint8_t *sQ = smem + L::kOffRing0;
+  uint8_t *sDO = smem + L::kOffRing1;
   uint8_t *sDS = smem + L::kOffDS;
 
-  if (warp < 4) {
-    regs_decrease<kRegsControl>();
-    if (warp == 0 && lane == 0) {
-      // ---------------------------------------------------------- producer
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -248,7 +244,7 @@ __global__ void __launch_bounds__(384, 1)
         const int st = t % S;
         if (!mbar_wait(&qdo_empty[st], ((t / S) & 1) ^ 1, ctl, kSiteDoEmpty)) break;
         mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile);
-        const int i = qblock(t);
+        const int i = i0 + t;
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s) {
           tma_load_3d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, i * kBlk, bh);
@@ -260,15 +256,16 @@ __global__ void __launch_bounds__(384, 1)
         mbar_drain(kv_full, 0);
         for (int t = (issued > S ? issued - S : 0); t < issued; ++t) mbar_drain(&qdo_full[t % S], (t / S) & 1);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
       constexpr uint32_t kIdescSq = idesc_bf16(kBlk, kBlk, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdescKB = idesc_bf16(kBlk, D, false, true);      // dV (TMEM A), dK
-      constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, true, true);        // dQ
+      constexpr uint32_t kIdescKV = idesc_bf16(kBlk, D, false, true);      // dV (TMEM A), dK
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aDO = smem_addr(sDO),
                      aDS = smem_addr(sDS);
-      const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
-                     tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDV = tmem + kColDV, tDK = tmem + kColDK;
+
       // S^T = K Q_t^T and dP^T = V dO_t^T (all operands K-major over d)
       auto issue_s = [&](int t) {
         const uint32_t q_base = aQ + (t % S) * L::kTile;
@@ -289,9 +286,6 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(dp_full);
       };
 
-      // Order per query block t:  dV_t, dQ_t, dK_t, S^T_{t+1}, dP^T_{t+1}.
-      // The row warps form P_{t+1} while dP^T_{t+1} runs and dS_{t+1} while
-      // dV_{t+1} runs; dQ_t drains while dK_t and S^T_{t+1} run.
       bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull) && mbar_wait(&qdo_full[0], 0, ctl, kSiteDoFull);
       if (ok) {
         tc_fence_after();
@@ -300,69 +294,59 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int t = 0; ok && t < n_q; ++t) {
         const int st = t % S;
-        const uint32_t q_base = aQ + st * L::kTile, do_base = aDO + st * L::kTile;
+        const bool more = t + 1 < n_q;
         // dV += P^T dO_t   (P^T from TMEM; dO_t is MN-major over d)
         if (!(ok = mbar_wait(p_ready, t & 1, ctl, kSitePReady))) break;
         tc_fence_after();
+        const uint32_t q_base = aQ + st * L::kTile, do_base = aDO + st * L::kTile;
 #pragma unroll 1
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_base + kk * 2048, kBlk * 128, 1024), kIdescKB, (t > 0 || kk > 0));
-        if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
-        if (!L::kDqAliasesDP && t > 0 && !(ok = mbar_wait(dq_empty, (t - 1) & 1, ctl, kSiteDqEmpty))) break;
-        tc_fence_after();
-        // dQ_t = dS K   (dS read MN-major from the dS^T tile; K MN-major over d)
-#pragma unroll 1
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tDQ, sdesc_sw128(aDS + kk * 2048, kBlk * 128, 1024), sdesc_sw128(aK + kk * 2048, kBlk * 128, 1024),
-                 kIdescQ, kk > 0);
-        tc_commit(dq_full);
+          mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_base + kk * 2048, kBlk * 128, 1024), kIdescKV, (t > 0 || kk > 0));
+        // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
+        // first, reads P^T(t) before S^T(t+1) overwrites it
+        if (more) {
+          if (!(ok = mbar_wait(&qdo_full[(t + 1) % S], ((t + 1) / S) & 1, ctl, kSiteDoFull))) break;
+          tc_fence_after();
+          issue_s(t + 1);
+        }
         // dK += dS^T Q_t   (dS^T K-major over queries; Q_t MN-major over d)
+        if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int kk = 0; kk < kBlk / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tDK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(q_base + kk * 2048, kBlk * 128, 1024), kIdescKB,
+          mma_ss(tDK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(q_base + kk * 2048, kBlk * 128, 1024), kIdescKV,
                  (t > 0 || kk > 0));
         }
         tc_commit(&qdo_empty[st]);
-        if (t + 1 < n_q) {
-          const int nst = (t + 1) % S;
-          if (!(ok = mbar_wait(&qdo_full[nst], ((t + 1) / S) & 1, ctl, kSiteDoFull))) break;
-          tc_fence_after();
-          issue_s(t + 1);
-          if (L::kDqAliasesDP) {
-            // dQ_t sits in the dP^T columns until it has been drained
-            if (!(ok = mbar_wait(dq_empty, t & 1, ctl, kSiteDqEmpty))) break;
-            tc_fence_after();
-          }
-          issue_dp(t + 1);
-        }
+        // dP^T(t+1): the rows have read dP^T(t) (ds_ready)
+        if (more) issue_dp(t + 1);
       }
       if (ok) tc_commit(acc_done);
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
-  } else if (warp < 8) {
-    regs_increase<kRegsRows>();
-    // ------------------------------------------------------------ P^T, dS^T (one key row per thread)
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ key rows
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the block
     const int key = jblk * kBlk + r;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + L::kColS + lane_base, tDP = tmem + L::kColDP + lane_base;
+    const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
     const int Np = nblk * kBlk;
     const float *lse2_h = p.lse2 + static_cast<size_t>(bh) * Np;
     const float *delta_h = p.delta + static_cast<size_t>(bh) * Np;
-    const uint32_t ds_row = smem_addr(sDS);
+    const uint32_t ds_tile = smem_addr(sDS);
+    const bool key_ok = key < N;
     bool ok = true;
 
     for (int t = 0; t < n_q; ++t) {
-      const int i = qblock(t);
+      const int i = i0 + t;
       // per-query statistics of this block (same for every thread: L1 broadcasts)
       const float4 *lse4 = reinterpret_cast<const float4 *>(lse2_h + i * kBlk);
       const float4 *del4 = reinterpret_cast<const float4 *>(delta_h + i * kBlk);
       const bool diag = CAUSAL && (i == jblk);
-      const bool key_ok = key < N;
 
       // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [0, 64).
       ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull);
@@ -433,100 +417,22 @@ __global__ void __launch_bounds__(384, 1)
           dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
           dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
         }
-        // dS^T row r, queries [32 ch, 32 ch + 32): four 16-byte chunks
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t addr = ds_row + sw128_offset(r, ch * 32 + u * 8, kBlk);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk[4 * u]), "r"(dk[4 * u + 1]),
-                       "r"(dk[4 * u + 2]), "r"(dk[4 * u + 3])
-                       : "memory");
-        }
+        store_row_sw128(ds_tile, r, ch * 32, dk);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
-    // dV epilogue
+    // dV and dK epilogues (the scale of dK applied here)
     if (ok) {
       ok = mbar_wait(acc_done, 0, ctl, kSiteMmaDone);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      __nv_bfloat16 *dst = p.dv + (static_cast<size_t>(bh) * N + key) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + L::kColDV + lane_base + ch * 32, v);
-        tmem_ld_wait(v);
-        if (key < N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
-        }
-      }
-    }
-  } else {
-    regs_decrease<kRegsDrain>();
-    // ------------------------------------------------------------ dQ drain (one query row per thread)
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tDQ = tmem + L::kColDQ + lane_base;
-    bool ok = true;
-    for (int t = 0; t < n_q; ++t) {
-      ok = mbar_wait(dq_full, t & 1, ctl, kSiteDqFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int q = qblock(t) * kBlk + r;
-      float4 *dst = reinterpret_cast<float4 *>(p.dq_acc + (static_cast<size_t>(bh) * N + q) * D);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tDQ + ch * 32, v);
-        tmem_ld_wait(v);
-        if (q < N) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            atomicAdd(dst + ch * 8 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-    }
-    // dK epilogue (scale applied here)
-    if (ok) {
-      ok = mbar_wait(acc_done, 0, ctl, kSiteMmaDone);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const int key = jblk * kBlk + r;
-      const float s = p.scale;
-      __nv_bfloat16 *dst = p.dk + (static_cast<size_t>(bh) * N + key) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + L::kColDK + lane_base + ch * 32, v);
-        tmem_ld_wait(v);
-        if (key < N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * s, __uint_as_float(v[8 * u + 1]) * s),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 2]) * s, __uint_as_float(v[8 * u + 3]) * s),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 4]) * s, __uint_as_float(v[8 * u + 5]) * s),
-                               pack_bf16x2(__uint_as_float(v[8 * u + 6]) * s, __uint_as_float(v[8 * u + 7]) * s));
-        }
-      }
+      const size_t row = static_cast<size_t>(bh) * N + key;
+      store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row * D, key_ok, 1.0f);
+      store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row * D, key_ok, p.scale);
     }
   }
 
@@ -538,45 +444,311 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ------------------------------------------------------------------ dQ
+
+// TMEM columns: S [0,128) (lane = query row), dP [128,256), dQ [256,256+D).
+// MMA order per key block j:  S(j+1), dP(j+1), dQ(j)
+// so the rows form P(j+1) while dP(j+1) and dQ(j) run and dS(j+1) while
+// S(j+2) runs.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr int S = L::kStages;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
+  uint64_t *qdo_full = bars;
+  uint64_t *kv_full = bars + 1;      // [S]
+  uint64_t *kv_empty = kv_full + S;  // [S]
+  uint64_t *s_full = kv_empty + S;
+  uint64_t *dp_full = s_full + 1;
+  uint64_t *s_free = dp_full + 1;
+  uint64_t *ds_ready = s_free + 1;
+  uint64_t *ds_free = ds_ready + 1;
+  uint64_t *dq_done = ds_free + 1;
+  uint64_t *drain = dq_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+  const WaitCtl ctl{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int nblk = p.num_blk;
+
+  // Tile order: causal puts the query blocks with the most key blocks
+  // (i large) first; otherwise the query blocks of one head run together.
+  int bh, iblk;
+  if (CAUSAL) {
+    iblk = nblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    bh = static_cast<int>(blockIdx.x) / nblk;
+    iblk = static_cast<int>(blockIdx.x) % nblk;
+  }
+  const int n_kv = CAUSAL ? (iblk + 1) : nblk;  // key blocks 0 .. n_kv-1
+
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(ds_ready, 128);
+    mbar_init(ds_free, 1);
+    mbar_init(dq_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t *sQ = smem + L::kOffRes0;
+  uint8_t *sDO = smem + L::kOffRes1;
+  uint8_t *sK = smem + L::kOffRing0;
+  uint8_t *sV = smem + L::kOffRing1;
+  uint8_t *sDS = smem + L::kOffDS;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(qdo_full, 2 * L::kTile);
+#pragma unroll
+      for (int s = 0; s < L::kSlabs; ++s) {
+        tma_load_3d(sQ + s * kBlk * 128, &tm_q, qdo_full, s * 64, iblk * kBlk, bh);
+        tma_load_3d(sDO + s * kBlk * 128, &tm_do, qdo_full, s * 64, iblk * kBlk, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % S;
+        if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1, ctl, kSiteKEmpty)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTile);
+#pragma unroll
+        for (int s = 0; s < L::kSlabs; ++s) {
+          tma_load_3d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &kv_full[st], s * 64, j * kBlk, bh);
+          tma_load_3d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &kv_full[st], s * 64, j * kBlk, bh);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(qdo_full, 0);
+        for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_drain(&kv_full[j % S], (j / S) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16(kBlk, kBlk, false, false);  // S, dP
+      constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, false, true);      // dQ
+      const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO), aK = smem_addr(sK), aV = smem_addr(sV),
+                     aDS = smem_addr(sDS);
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ;
+
+      // S = Q K_j^T and dP = dO V_j^T (all operands K-major over d)
+      auto issue_s = [&](int j) {
+        const uint32_t k_base = aK + (j % S) * L::kTile;
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
+          mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0);
+        }
+        tc_commit(s_full);
+      };
+      auto issue_dp = [&](int j) {
+        const uint32_t v_base = aV + (j % S) * L::kTile;
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
+          mma_ss(tDP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(v_base + off, 16, 1024), kIdescS, kk > 0);
+        }
+        tc_commit(dp_full);
+      };
+
+      bool ok = mbar_wait(qdo_full, 0, ctl, kSiteQFull) && mbar_wait(&kv_full[0], 0, ctl, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % S;
+        const bool more = j + 1 < n_kv;
+        if (more) {
+          // S(j+1) once the rows have read S(j)
+          if (!(ok = mbar_wait(&kv_full[(j + 1) % S], ((j + 1) / S) & 1, ctl, kSiteKFull))) break;
+          if (!(ok = mbar_wait(s_free, j & 1, ctl, kSiteSFull))) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        // dP(j+1) once the rows have read dP(j); dQ(j) once dS(j) is in smem
+        if (!(ok = mbar_wait(ds_ready, j & 1, ctl, kSiteDsReady))) break;
+        tc_fence_after();
+        if (more) issue_dp(j + 1);
+        // dQ += dS K_j   (dS K-major over keys; K_j MN-major over d)
+        const uint32_t k_base = aK + st * L::kTile;
+#pragma unroll 1
+        for (int kk = 0; kk < kBlk / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
+          mma_ss(tDQ, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(k_base + kk * 2048, kBlk * 128, 1024), kIdescQ,
+                 (j > 0 || kk > 0));
+        }
+        tc_commit(ds_free);
+        tc_commit(&kv_empty[st]);
+      }
+      if (ok) tc_commit(dq_done);
+      tc_commit(drain);
+      mbar_drain(drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ query rows
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row within the block
+    const int qrow = iblk * kBlk + r;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
+    const float c = p.scale_log2;
+    const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + qrow;
+    const float lse2 = p.lse2[srow];  // +inf on padding rows: P = 0
+    const float dlt = p.delta[srow];
+    const uint32_t ds_tile = smem_addr(sDS);
+    const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
+    bool ok = true;
+
+    for (int j = 0; j < n_kv; ++j) {
+      const bool diag = CAUSAL && (j == iblk);
+      // Phase 1: P = exp2(S c - lse2), kept as bf16 pairs.
+      ok = mbar_wait(s_full, j & 1, ctl, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pk[64];
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) {
+        uint32_t sv[32];
+        tmem_ld32(tS + ch * 32, sv);
+        tmem_ld_wait(sv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
+          float p0 = ex2(x.x), p1 = ex2(x.y);
+          if (diag) {  // key kc visible to query r iff kc <= r
+            p0 = (ch * 32 + e <= r) ? p0 : 0.0f;
+            p1 = (ch * 32 + e + 1 <= r) ? p1 : 0.0f;
+          }
+          pk[ch * 16 + e / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+
+      // Phase 2: dS = P o (dP - D) -> bf16 into the swizzled [query][key] tile.
+      ok = mbar_wait(dp_full, j & 1, ctl, kSiteSFull);
+      if (ok && j > 0) ok = mbar_wait(ds_free, (j - 1) & 1, ctl, kSiteDsReady);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) {
+        uint32_t dpv[32];
+        tmem_ld32(tDP + ch * 32, dpv);
+        tmem_ld_wait(dpv);
+        uint32_t dsv[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const uint32_t pp = pk[ch * 16 + e / 2];
+          const float2 g = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd);
+          const float2 ds =
+              ffma2(make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)), g, make_float2(0.f, 0.f));
+          dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
+        }
+        store_row_sw128(ds_tile, r, ch * 32, dsv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // dQ epilogue (the scale applied here)
+    if (ok) {
+      ok = mbar_wait(dq_done, 0, ctl, kSiteMmaDone);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      store_acc_row<D>(tmem + kColDQ + lane_base, p.dq + (static_cast<size_t>(bh) * N + qrow) * D, qrow < N,
+                       p.scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename Kern>
+cudaError_t launch_main(Kern kern, unsigned grid, uint32_t smem, const CUtensorMap &tq, const CUtensorMap &tk,
+                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
-                         const BwdParams &p, cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+                         const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
   using L = BwdLayout<D>;
-  const long long rows = static_cast<long long>(p.BH) * p.N;
   const long long padded_rows = static_cast<long long>(p.BH) * p.num_blk * kBlk;
   constexpr int kRowsPerBlock = 256 / (D / 8);
   fa_bwd_pre_kernel<D>
       <<<static_cast<unsigned>((padded_rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-
-  auto kern = fa_bwd_main_kernel<D, CAUSAL>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
+  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);
+  if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
+  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
-  if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk), 384, L::kSmemRequest, stream>>>(tq, tk, tv,
-                                                                                                       tdo, p);
-  e = cudaGetLastError();
+  if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
+  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
-  if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return e;
-
-  const long long n4 = rows * D / 4;
-  long long blocks = (n4 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, cudaEvent_t ev_start,
-                       cudaEvent_t ev_stop) {
+                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
   if (d == 64)
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop);
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream, ev_start, ev_stop);
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream, ev)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream, ev);
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream, ev)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream, ev);
 }
 
 }  // namespace fa

@@ -45,7 +45,6 @@ struct BwdParams {
   const float *lse;           // [BH, N]
   float *delta;               // [BH, Np]  D = rowsum(dO * O), Np = 128 * num_blk, 0 past N
   float *lse2;                // [BH, Np]  lse * log2(e), +inf past N
-  float *dq_acc;              // [BH, N, d] fp32
   __nv_bfloat16 *dq;          // [BH, N, d]
   __nv_bfloat16 *dk;          // [BH, N, d]
   __nv_bfloat16 *dv;          // [BH, N, d]
@@ -62,9 +61,10 @@ struct BwdParams {
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 
-// ev_start/ev_stop (may be null) are recorded around the main kernel.
+// ev[0..2] (all null or all set) are recorded before the dK/dV kernel,
+// between it and the dQ kernel, and after the dQ kernel.
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
-                       cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+                       cudaStream_t stream, const cudaEvent_t *ev);
 
 }  // namespace fa

@@ -76,10 +76,9 @@ FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, 
                    cudaStream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
- * accumulator [B, H, N, d], plus D = rowsum(dO * O) and the logsumexp in
- * log2 units, each fp32 [B, H, Np] with N padded up to Np, the next
- * multiple of 128; each part rounded up to 256 bytes.  Linear in N.
+ * Bytes of device workspace fa_bwd needs for these sizes: D = rowsum(dO * O)
+ * and the logsumexp in log2 units, each fp32 [B, H, Np] with N padded up to
+ * Np, the next multiple of 128, each rounded up to 256 bytes.  Linear in N.
  * Returns 0 for sizes fa_bwd would reject.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -96,9 +95,7 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace      : device scratch of at least fa_bwd_workspace_bytes()
  *                    bytes, 256-byte aligned, or NULL to let the library
  *                    take it with cudaMallocAsync/cudaFreeAsync on `stream`.
- * dq is accumulated with fp32 atomics across key blocks, so it is not
- * bitwise reproducible run to run (differences stay at fp32 rounding level
- * before the bf16 cast).  dk and dv are reproducible.
+ * No atomics are used: dq, dk and dv are bitwise reproducible run to run.
  */
 FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
                    const void *dO, const float *lse, void *dq, void *dk, void *dv,
@@ -122,14 +119,14 @@ FA_API int fa_debug_last_wait_site(void);
 
 /*
  * Diagnostic timing hook: the next fa_bwd call made by this host thread
- * records `start` on its stream right before the launch of its main kernel
- * (the one that recomputes the probabilities and forms dQ, dK, dV) and
- * `stop` right after it, so that kernel can be timed with
+ * records, on its stream, `start` right before the launch of its dK/dV
+ * kernel, `mid` between that kernel and its dQ kernel, and `stop` right
+ * after the dQ kernel, so both kernels can be timed with
  * cudaEventElapsedTime.  The events are created and owned by the caller;
  * the hook is used once and then cleared.  Returns FA_ERR_INVALID_ARGUMENT
- * if either event is NULL.
+ * if any event is NULL.
  */
-FA_API fa_status_t fa_debug_time_next_bwd_main(cudaEvent_t start, cudaEvent_t stop);
+FA_API fa_status_t fa_debug_time_next_bwd(cudaEvent_t start, cudaEvent_t mid, cudaEvent_t stop);
 
 /* A static, NUL-terminated description of a status code. */
 FA_API const char *fa_status_string(fa_status_t status);

@@ -50,6 +50,8 @@ def _bind(path: str):
     lib.oracle_bwd.restype = I
     lib.oracle_probs.argtypes = [dp, dp, dp, L, L, L, I, D]
     lib.oracle_probs.restype = I
+    lib.oracle_fwd_spread.argtypes = [dp, dp, dp, dp, L, L, L, L, I, D, I]
+    lib.oracle_fwd_spread.restype = I
     return lib
 
 
@@ -139,3 +141,18 @@ def probs(q, k, causal: bool, scale: float, lib=None):
     if rc != 0:
         raise RuntimeError(f"oracle_probs failed ({rc})")
     return p
+
+
+def fwd_spread(q, k, v, causal: bool, scale: float, nthreads: int | None = None, lib=None):
+    """spread[..., i, c] = sum_j P_ij |v_jc - O_ic| (fp64).
+
+    A relative perturbation e of every weight P_ij moves O_ic by at most
+    e * spread; used to derive the O tolerance for short-format weights."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lead, BH, Nq, Nk, d = _shape(q, k)
+    out = np.empty(q.shape, np.float64)
+    rc = (lib or _load()).oracle_fwd_spread(_ptr(q), _ptr(k), _ptr(v), _ptr(out), BH, Nq, Nk, d,
+                                            int(bool(causal)), float(scale), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_fwd_spread failed ({rc})")
+    return out

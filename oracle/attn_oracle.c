@@ -295,6 +295,57 @@ int oracle_bwd(const double *q, const double *k, const double *v,
     return rc;
 }
 
+/* Rounding spread of the output: spread[h][i][c] = sum_j P_ij |v_jc - O_ic|
+ * with P and O as above.  It bounds how far O can move when every weight
+ * P_ij is perturbed by a relative amount e: |dO_ic| <= e * spread[h][i][c]
+ * (the weights still summing to one), which is what rounding the weights to
+ * a short format does.  Test infrastructure for deriving tolerances. */
+static void *spread_worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    long d = J->d;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!p || !o) { free(p); free(o); return (void *)1; }
+    long item;
+    while (take_item(J, &item)) {
+        long h = item / J->items_per_head;
+        long r0 = (item % J->items_per_head) * J->rows_per_item;
+        long r1 = r0 + J->rows_per_item;
+        if (r1 > J->Nq) r1 = J->Nq;
+        const double *kh = J->k + h * J->Nk * d;
+        const double *vh = J->v + h * J->Nk * d;
+        for (long i = r0; i < r1; ++i) {
+            long end = visible_end(J, i);
+            double M, Z;
+            softmax_row(J, J->q + (h * J->Nq + i) * d, kh, end, p, &M, &Z);
+            for (long c = 0; c < d; ++c) o[c] = 0.0;
+            for (long j = 0; j < end; ++j)
+                for (long c = 0; c < d; ++c) o[c] += p[j] * vh[j * d + c];
+            double *si = J->o + (h * J->Nq + i) * d;   /* the spread output */
+            for (long c = 0; c < d; ++c) si[c] = 0.0;
+            for (long j = 0; j < end; ++j)
+                for (long c = 0; c < d; ++c) si[c] += p[j] * fabs(vh[j * d + c] - o[c]);
+        }
+    }
+    free(p);
+    free(o);
+    return NULL;
+}
+
+int oracle_fwd_spread(const double *q, const double *k, const double *v,
+                      double *spread, long BH, long Nq, long Nk, long d,
+                      int causal, double scale, int nthreads)
+{
+    if (check_args(BH, Nq, Nk, d, causal) || !q || !k || !v || !spread) return -1;
+    job_t J;
+    init_job(&J, BH, Nq, Nk, d, causal, scale, nthreads);
+    J.q = q; J.k = k; J.v = v; J.o = spread;
+    int rc = run_threads(&J, spread_worker, nthreads);
+    pthread_mutex_destroy(&J.mu);
+    return rc;
+}
+
 /* The normalised probability matrix P[Nq][Nk] of one head (zeros where the
  * mask hides a key).  For small cases only: it is O(Nq*Nk) memory. */
 int oracle_probs(const double *q, const double *k, double *p, long Nq, long Nk,

@@ -228,6 +228,30 @@ def pin_library_sdpa(lib=None):
         np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
 
 
+def pin_spread(lib=None):
+    """spread = sum_j P_ij |v_j - O_i|: 0 for constant V; for uniform weights
+    over values +-1 (mean 0) it is 1; and it bounds the change of O when the
+    weights are perturbed by a relative e and renormalised."""
+    q, k, v, _ = _qkv(31, 2, 12, 5)
+    v[:] = 0.7
+    assert np.max(np.abs(oracle.fwd_spread(q, k, v, False, 0.4, lib=lib))) <= 1e-15
+    q0 = np.zeros((1, 8, 3))
+    v1 = np.tile(np.array([1.0, -1.0])[:, None], (4, 3))[None]
+    np.testing.assert_allclose(oracle.fwd_spread(q0, _qkv(32, 1, 8, 3)[1], v1, False, 1.0, lib=lib), 1.0,
+                               atol=1e-14)
+    # perturbation bound, checked by brute force on one head
+    q, k, v, _ = _qkv(33, 1, 9, 4)
+    P = oracle.probs(q[0], k[0], False, 0.9, lib=lib)
+    sp = oracle.fwd_spread(q, k, v, False, 0.9, lib=lib)[0]
+    e = 1e-3
+    r = _rng(34)
+    for _ in range(20):
+        Pt = P * (1 + e * r.uniform(-1, 1, P.shape))
+        Pt /= Pt.sum(1, keepdims=True)
+        dO = np.abs(Pt @ v[0] - P @ v[0])
+        assert np.all(dO <= 2 * e * sp + 1e-15)
+
+
 ALL_PINS = [
     pin_hand_example,
     pin_rows_sum_to_one,
@@ -242,4 +266,5 @@ ALL_PINS = [
     pin_finite_differences_all,
     pin_finite_differences_sampled,
     pin_library_sdpa,
+    pin_spread,
 ]

@@ -60,13 +60,16 @@ def _run(w, heads_max=4, full_torch=True):
     of, lsef = o.view(w.B * w.H, w.N, w.d), lse.view(w.B * w.H, w.N)
     for hh in heads:
         o_ref, lse_ref = oracle.fwd(qf[hh], kf[hh], vf[hh], w.causal, w.scale)
-        check_o(of[hh], o_ref, f"{w.name} head {hh}")
+        spread = oracle.fwd_spread(qf[hh], kf[hh], vf[hh], w.causal, w.scale)
+        check_o(of[hh], o_ref, f"{w.name} head {hh}", spread)
         check_lse(lsef[hh], lse_ref, f"{w.name} head {hh}")
         if grads is not None:
             refs = oracle.bwd(qf[hh], kf[hh], vf[hh], dof[hh], w.causal, w.scale)
             for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
                 check_grad(g.view(w.B * w.H, w.N, w.d)[hh], r, name, f"{w.name} head {hh}")
     if full_torch:
+        # every head against PyTorch fp32 attention on the GPU (flat bound;
+        # used on workloads with unit-variance inputs only)
         o_t, lse_t = _torch_ref_fwd(q, k, v, w.causal, w.scale)
         err = (o.float() - o_t).abs()
         bound = torch.clamp(0.5 * torch.exp2(torch.floor(torch.log2(o_t.abs().clamp_min(1e-30)))) / 128 + 2e-3,

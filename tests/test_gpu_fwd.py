@@ -38,9 +38,13 @@ def test_fwd_small(N, d, causal):
 
 @pytest.mark.parametrize("scale", [-0.3, 0.0, 0.5])
 def test_fwd_scale_values(scale):
+    """Negative, zero and a large scale (0.5 at d = 64: logits of std 4, a
+    very sharp softmax, checked with the bound derived from bf16 weights)."""
     for causal in (False, True):
         o, lse, o_ref, lse_ref = _run(1, 2, 200, 64, causal, scale=scale, seed=3)
-        check_o(o, o_ref, f"scale={scale}")
+        q, k, v, _ = draw_shape(1, 2, 200, 64, 3, 1.0, "cpu", torch.bfloat16, with_dout=False)
+        spread = oracle.fwd_spread(q, k, v, causal, scale)
+        check_o(o, o_ref, f"scale={scale}", spread)
         check_lse(lse, lse_ref, f"scale={scale}")
 
 
