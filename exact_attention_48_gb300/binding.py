@@ -55,6 +55,8 @@ def library(path: str | None = None):
             lib.fa_bwd_workspace_bytes.restype = sz
             lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
             lib.fa_bwd.restype = i
+            lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            lib.fa_bwd_noalloc.restype = i
             lib.fa_device_status.argtypes = [vp]
             lib.fa_device_status.restype = i
             lib.fa_debug_last_wait_site.argtypes = []
@@ -151,6 +153,31 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
                           _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+                   dq=None, dk=None, dv=None, stream=None):
+    """fa_bwd for callers that cannot allocate device memory: the library's
+    fixed scratch array replaces the workspace (see include/fa.h)."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    rc = library().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                  lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                  B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -103,6 +103,42 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Size in bytes of the fixed device array that fa_bwd_noalloc uses as its
+ * scratch (8 MiB).  Every GPU that loads the library holds this array until
+ * the process exits.  It covers B * H * Np <= 1,048,576 padded rows, where
+ * Np is N rounded up to a multiple of 128 (for example B*H = 32 heads of
+ * N = 32768).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * Backward pass for callers that must not allocate device memory: the same
+ * computation, arguments, layouts and results as fa_bwd, but with no
+ * workspace argument and no allocation of any kind (no cudaMalloc,
+ * cudaMallocAsync or cudaFree).  Its scratch lives in a fixed array of the
+ * library (FA_NOALLOC_SCRATCH_BYTES); calls that would need more return
+ * FA_ERR_WORKSPACE without launching anything.
+ *
+ * Who needs it: callers whose device memory is owned by someone else (a
+ * framework's memory manager that must see every allocation) or planned up
+ * front (a process that must not allocate once it runs), which can neither
+ * pass fa_bwd a workspace nor let it take one.
+ *
+ * Set-up and sharing: the first call on a device, with that device current,
+ * looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the last call's contents; nothing in it needs to start at zero.
+ * Calls whose work overlaps on the GPU (other streams or host threads on
+ * the same device) race on it, so the caller must order them.
+ *
+ * The pages describe no counterpart of this entry point.
+ */
+FA_API fa_status_t fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                  const void *dO, const float *lse, void *dq, void *dk, void *dv,
+                                  int B, int H, int N, int d, int causal, float scale,
+                                  cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns the status word the kernels of the
  * current device recorded (FA_OK or FA_ERR_DEVICE_TIMEOUT) and resets it to
  * FA_OK.  Returns FA_ERR_CUDA if the synchronisation itself fails.
