@@ -149,9 +149,10 @@ struct BwdLayout {
 // dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The products are
 // formed transposed (S^T = K Q^T, dP^T = V dO^T) so the key row, which owns
 // dK and dV, is the TMEM lane.  MMA order per query block t:
-//   dV(t), S^T(t+1), dK(t), dP^T(t+1)
-// so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
-// dV(t+1) and S^T(t+2) run.
+//   dV(t), S^T(t+1), [dK(t) | dP^T(t+1)]
+// ([a | b]: the MMAs of two products with different accumulators issued
+// alternately) so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and
+// dS^T(t+1) while dV(t+1) and S^T(t+2) run.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -266,31 +267,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                      aDS = smem_addr(sDS);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDV = tmem + kColDV, tDK = tmem + kColDK;
 
-      // S^T = K Q_t^T and dP^T = V dO_t^T (all operands K-major over d)
-      auto issue_s = [&](int t) {
-        const uint32_t q_base = aQ + (t % S) * L::kTile;
-#pragma unroll 1
+      // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
+      // a compile-time step offset (all issue loops are unrolled).
+      const uint64_t dK = sdesc_sw128(aK, 16, 1024), dV = sdesc_sw128(aV, 16, 1024);
+      const uint64_t dDS = sdesc_sw128(aDS, 16, 1024);
+      auto q_kmaj = [&](int t) { return sdesc_sw128(aQ + (t % S) * L::kTile, 16, 1024); };
+      auto q_mn = [&](int t) { return sdesc_sw128(aQ + (t % S) * L::kTile, kBlk * 128, 1024); };
+      auto do_kmaj = [&](int t) { return sdesc_sw128(aDO + (t % S) * L::kTile, 16, 1024); };
+      auto do_mn = [&](int t) { return sdesc_sw128(aDO + (t % S) * L::kTile, kBlk * 128, 1024); };
+
+      // S^T(t) = K Q_t^T and dP^T(t) = V dO_t^T (all operands K-major over
+      // d), interleaved: two independent accumulators keep the tensor pipe
+      // full where one dependent chain runs at about half rate.
+      auto issue_s_dp = [&](int t) {
+        const uint64_t bq = q_kmaj(t), bdo = do_kmaj(t);
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), kIdescSq, kk > 0);
+          mma_ss(tS, desc_add(dK, kmajor_step(kk, kBlk)), desc_add(bq, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
+          mma_ss(tDP, desc_add(dV, kmajor_step(kk, kBlk)), desc_add(bdo, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
         }
         tc_commit(s_full);
-      };
-      auto issue_dp = [&](int t) {
-        const uint32_t do_base = aDO + (t % S) * L::kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tDP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024), kIdescSq, kk > 0);
-        }
         tc_commit(dp_full);
+      };
+      auto issue_s = [&](int t) {
+        const uint64_t bq = q_kmaj(t);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, desc_add(dK, kmajor_step(kk, kBlk)), desc_add(bq, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
+        tc_commit(s_full);
       };
 
       bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull) && mbar_wait(&qdo_full[0], 0, ctl, kSiteDoFull);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
+        issue_s_dp(0);
       }
       for (int t = 0; ok && t < n_q; ++t) {
         const int st = t % S;
@@ -298,10 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV += P^T dO_t   (P^T from TMEM; dO_t is MN-major over d)
         if (!(ok = mbar_wait(p_ready, t & 1, ctl, kSitePReady))) break;
         tc_fence_after();
-        const uint32_t q_base = aQ + st * L::kTile, do_base = aDO + st * L::kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tDV, tS + kk * 8, sdesc_sw128(do_base + kk * 2048, kBlk * 128, 1024), kIdescKV, (t > 0 || kk > 0));
+        {
+          const uint64_t bdo = do_mn(t);
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tDV, tS + kk * 8, desc_add(bdo, mnmajor_step(kk)), kIdescKV, (t > 0 || kk > 0));
+        }
         // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
         // first, reads P^T(t) before S^T(t+1) overwrites it
         if (more) {
@@ -309,18 +321,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(t + 1);
         }
-        // dK += dS^T Q_t   (dS^T K-major over queries; Q_t MN-major over d)
+        // dK += dS^T Q_t (dS^T K-major over queries; Q_t MN-major over d),
+        // interleaved with dP^T(t+1) once the rows have read dP^T(t)
         if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kBlk / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tDK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(q_base + kk * 2048, kBlk * 128, 1024), kIdescKV,
-                 (t > 0 || kk > 0));
+        {
+          const uint64_t bq = q_mn(t), bdo = more ? do_kmaj(t + 1) : 0;
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            mma_ss(tDK, desc_add(dDS, kmajor_step(kk, kBlk)), desc_add(bq, mnmajor_step(kk)), kIdescKV,
+                   (t > 0 || kk > 0));
+            if (more && kk < D / 16)
+              mma_ss(tDP, desc_add(dV, kmajor_step(kk, kBlk)), desc_add(bdo, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
+          }
         }
         tc_commit(&qdo_empty[st]);
-        // dP^T(t+1): the rows have read dP^T(t) (ds_ready)
-        if (more) issue_dp(t + 1);
+        if (more) tc_commit(dp_full);
       }
       if (ok) tc_commit(acc_done);
       tc_commit(drain);
@@ -447,9 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ dQ
 
 // TMEM columns: S [0,128) (lane = query row), dP [128,256), dQ [256,256+D).
-// MMA order per key block j:  S(j+1), dP(j+1), dQ(j)
-// so the rows form P(j+1) while dP(j+1) and dQ(j) run and dS(j+1) while
-// S(j+2) runs.
+// MMA order per key block j:  S(j+1), [dQ(j) | dP(j+1)]
+// ([a | b]: the MMAs of two products with different accumulators issued
+// alternately) so the rows form P(j+1) while dQ(j) and dP(j+1) run and
+// dS(j+1) while S(j+2) runs.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -563,31 +580,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                      aDS = smem_addr(sDS);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ;
 
-      // S = Q K_j^T and dP = dO V_j^T (all operands K-major over d)
+      // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
+      // a compile-time step offset (all issue loops are unrolled).
+      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dDO = sdesc_sw128(aDO, 16, 1024);
+      const uint64_t dDS = sdesc_sw128(aDS, 16, 1024);
+      auto k_kmaj = [&](int j) { return sdesc_sw128(aK + (j % S) * L::kTile, 16, 1024); };
+      auto k_mn = [&](int j) { return sdesc_sw128(aK + (j % S) * L::kTile, kBlk * 128, 1024); };
+      auto v_kmaj = [&](int j) { return sdesc_sw128(aV + (j % S) * L::kTile, 16, 1024); };
+
+      // S(j) = Q K_j^T (both K-major over d)
       auto issue_s = [&](int j) {
-        const uint32_t k_base = aK + (j % S) * L::kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0);
-        }
+        const uint64_t bk = k_kmaj(j);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, desc_add(dQ, kmajor_step(kk, kBlk)), desc_add(bk, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
         tc_commit(s_full);
       };
-      auto issue_dp = [&](int j) {
-        const uint32_t v_base = aV + (j % S) * L::kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tDP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(v_base + off, 16, 1024), kIdescS, kk > 0);
-        }
-        tc_commit(dp_full);
+      // dP(j) = dO V_j^T (K-major over d), alone or interleaved with dQ += dS K
+      auto dp_step = [&](uint64_t bv, int kk) {
+        mma_ss(tDP, desc_add(dDO, kmajor_step(kk, kBlk)), desc_add(bv, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
       };
 
       bool ok = mbar_wait(qdo_full, 0, ctl, kSiteQFull) && mbar_wait(&kv_full[0], 0, ctl, kSiteKFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
+        const uint64_t bv = v_kmaj(0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
+        tc_commit(dp_full);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % S;
@@ -599,18 +620,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(j + 1);
         }
-        // dP(j+1) once the rows have read dP(j); dQ(j) once dS(j) is in smem
+        // dQ += dS K_j (dS K-major over keys; K_j MN-major over d) once dS(j)
+        // is in smem, interleaved with dP(j+1) (the rows have read dP(j))
         if (!(ok = mbar_wait(ds_ready, j & 1, ctl, kSiteDsReady))) break;
         tc_fence_after();
-        if (more) issue_dp(j + 1);
-        // dQ += dS K_j   (dS K-major over keys; K_j MN-major over d)
-        const uint32_t k_base = aK + st * L::kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < kBlk / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-          mma_ss(tDQ, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(k_base + kk * 2048, kBlk * 128, 1024), kIdescQ,
-                 (j > 0 || kk > 0));
+        {
+          const uint64_t bk = k_mn(j), bv = more ? v_kmaj(j + 1) : 0;
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            mma_ss(tDQ, desc_add(dDS, kmajor_step(kk, kBlk)), desc_add(bk, mnmajor_step(kk)), kIdescQ,
+                   (j > 0 || kk > 0));
+            if (more && kk < D / 16) dp_step(bv, kk);
+          }
         }
+        if (more) tc_commit(dp_full);
         tc_commit(ds_free);
         tc_commit(&kv_empty[st]);
       }

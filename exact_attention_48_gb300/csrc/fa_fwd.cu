@@ -355,15 +355,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
       // TMEM columns of tile t: S at t*128, O at 256 + t*D
 
+      // Descriptors: the Q tiles once, K/V per stage; every MMA adds a
+      // compile-time step offset (the issue loops are unrolled).
+      const uint64_t dQ0 = sdesc_sw128(aQ, 16, 1024), dQ1 = sdesc_sw128(aQ + L::kQTile, 16, 1024);
+
       // S_t = Q_t K_j^T (both operands K-major over d)
       auto issue_s = [&](int t, int j) {
-        const uint32_t kbase = aK + (j % S) * L::kKVBytes, qbase = aQ + t * L::kQTile;
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qbase + koff, 16, 1024), sdesc_sw128(kbase + koff, 16, 1024), kIdescS,
+        const uint64_t bq = t ? dQ1 : dQ0, bk = sdesc_sw128(aK + (j % S) * L::kKVBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + t * 128, desc_add(bq, kmajor_step(kk, kBM)), desc_add(bk, kmajor_step(kk, kBN)), kIdescS,
                  kk > 0 ? 1u : 0u);
-        }
         tc_commit(&s_full[t]);
       };
       // O_t += P_t V_j; P_t sits (bf16, two per column) over S_t in TMEM and
@@ -372,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t, int j) -> bool {
         if (!mbar_wait(&p_ready[t], j & 1, ctl, kSitePReady)) return false;
         tc_fence_after();
-        const uint32_t vbase = aV + (j % S) * L::kKVBytes;
-#pragma unroll 1
+        const uint64_t bv = sdesc_sw128(aV + (j % S) * L::kKVBytes, kBN * 128, 1024);
+#pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(vbase + kk * 2048, kBN * 128, 1024), kIdescO,
+          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(bv, mnmajor_step(kk)), kIdescO,
                  (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[t]);
         return true;

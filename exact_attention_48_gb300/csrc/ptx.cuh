@@ -103,24 +103,29 @@ struct WaitCtl {
   int *status;               // global: [0] = status code, [1] = site of the first timeout
 };
 
-constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;  // 1.5 s per wait
-constexpr int kStatusTimeout = 5;                                // FA_ERR_DEVICE_TIMEOUT
+constexpr long long kWaitLimitCycles = 3000000000LL;  // ~1.5 s at 2 GHz
+constexpr int kStatusTimeout = 5;                      // FA_ERR_DEVICE_TIMEOUT
 
-// Wait for the phase of `bar` with parity `parity` to complete.  Gives up
-// after kWaitLimitNs or as soon as another role of the CTA has given up;
-// returns false then (and records the first timeout in the status word).
+// Wait for the phase of `bar` with parity `parity` to complete.  Polls with
+// try_wait (which suspends the thread until the phase completes or a short
+// hardware limit passes); every 256 polls it checks whether another role of
+// the CTA has given up and whether kWaitLimitCycles SM cycles have passed.
+// Returns false on either (and records the first timeout in the status
+// word).  The SM cycle counter is used rather than the global timer because
+// it is cheap to read.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &ctl, int site) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  const long long t0 = clock64();
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*ctl.abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *ctl.abort_flag = 1;
-      if (atomicCAS(ctl.status, 0, kStatusTimeout) == 0) atomicExch(ctl.status + 1, site);
-      return false;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*ctl.abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *ctl.abort_flag = 1;
+        if (atomicCAS(ctl.status, 0, kStatusTimeout) == 0) atomicExch(ctl.status + 1, site);
+        return false;
+      }
     }
   }
 }
@@ -128,10 +133,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 // Same, without consulting the abort flag: used on the way out to drain
 // asynchronous copies and MMAs that are still in flight.
 __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+  const long long t0 = clock64();
+#pragma unroll 1
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 255u && clock64() - t0 > kWaitLimitCycles) return false;
+  }
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -239,6 +246,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, ui
   d |= 2ull << 61;  // 128-byte swizzle
   return d;
 }
+
+// A descriptor moved by `bytes` inside its tile.  Shared-memory addresses
+// stay below 256 KB, so the 14-bit start field never carries into the
+// leading-dimension field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// Byte offset of the kk-th K step (16 bf16 = 32 bytes) of a K-major
+// 128-byte-swizzled tile of 64-column slabs with `rows` rows: inside a
+// slab the step moves 32 bytes along the 128-byte row; every 4 steps the
+// next slab starts.
+__host__ __device__ constexpr uint32_t kmajor_step(int kk, int rows) {
+  return static_cast<uint32_t>((kk >> 2) * (rows * 128) + (kk & 3) * 32);
+}
+
+// Byte offset of the kk-th K step (16 rows) of an MN-major tile: two
+// 1024-byte groups of 8 rows.
+__host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return static_cast<uint32_t>(kk * 2048); }
 
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 //   M in {64, 128, 256}, N a multiple of 16 in [16, 256];
