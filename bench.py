@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time fwd and bwd separately over the sequence-length sweep (one JSON line per point)")
     return ap.parse_args()
 
 
@@ -404,8 +406,56 @@ def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
             "steps": steps}
 
 
+def run_sweep(args):
+    """B*N = 16384 tokens, H = 16, N in 512..16384, d in {64, 128}, causal and
+    not: forward and backward timed separately with CUDA events (median of
+    args.steps after args.warmup), one JSON line per point."""
+    import torch
+    from exact_attention_48_gb300 import fa_bwd, fa_bwd_workspace_bytes, fa_fwd
+    from exact_attention_48_gb300.inputs import SWEEP_N, draw, sweep
+    peaks, peak_src = load_peaks()
+    steps = max(5, min(args.steps, 50))
+    for d in (64, 128):
+        for causal in (False, True):
+            for N in SWEEP_N:
+                w = sweep(N, d, causal)
+                q, k, v, do = draw(w, device="cuda")
+                o, lse = fa_fwd(q, k, v, causal, w.scale)
+                ws = torch.empty(fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+                for _ in range(max(3, args.warmup)):
+                    fa_fwd(q, k, v, causal, w.scale, o=o, lse=lse)
+                    fa_bwd(q, k, v, o, do, lse, causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+                tf, tb = [], []
+                for _ in range(steps):
+                    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    e[0].record()
+                    fa_fwd(q, k, v, causal, w.scale, o=o, lse=lse)
+                    e[1].record()
+                    fa_bwd(q, k, v, o, do, lse, causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+                    e[2].record()
+                    torch.cuda.synchronize()
+                    tf.append(e[0].elapsed_time(e[1]))
+                    tb.append(e[1].elapsed_time(e[2]))
+                mf, mb = statistics.median(tf), statistics.median(tb)
+                ftf = w.flops_fwd() / (mf * 1e-3) / 1e12
+                btf = w.flops_bwd() / (mb * 1e-3) / 1e12
+                # algorithmic HBM bytes of the forward: q, k, v read, o written, lse written
+                fbytes = 8.0 * w.B * w.H * w.N * w.d + 4.0 * w.B * w.H * w.N
+                print(json.dumps({"sweep": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "causal": causal,
+                                  "fwd_ms": mf, "fwd_tflops": ftf, "fwd_frac_of_sustained": ftf / peaks["bf16_tflops_sustained"],
+                                  "bwd_ms": mb, "bwd_tflops": btf, "bwd_frac_of_sustained": btf / peaks["bf16_tflops_sustained"],
+                                  "fwd_hbm_gbs_algorithmic": fbytes / (mf * 1e-3) / 1e9, "peak_source": peak_src}),
+                      flush=True)
+                del q, k, v, do, o, lse, ws, dq, dk, dv
+                torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -372,11 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint32_t pk[64];  // P^T row, bf16 pairs, kept for phase 2
+      uint32_t sva[4][32];
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tS + ch * 32, sva[ch]);
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(sva[ch]);
 #pragma unroll
       for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t sv[32];
-        tmem_ld32(tS + ch * 32, sv);
-        tmem_ld_wait(sv);
+        const uint32_t(&sv)[32] = sva[ch];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int qc = ch * 32 + e;  // query column within the block
@@ -411,11 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      uint32_t dpa[4][32];
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tDP + ch * 32, dpa[ch]);
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(dpa[ch]);
 #pragma unroll
       for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t dpv[32];
-        tmem_ld32(tDP + ch * 32, dpv);
-        tmem_ld_wait(dpv);
+        const uint32_t(&dpv)[32] = dpa[ch];
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -462,33 +468,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ dQ
 
-// TMEM columns: S [0,128) (lane = query row), dP [128,256), dQ [256,256+D).
+template <int D>
+struct DqLayout {
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr uint32_t kTile = kBlk * D * 2;  // one [128][D] bf16 tile
+  // Q resident, K in a 3-stage ring, V in a 2-stage ring, one [128][128]
+  // bf16 dS tile.  dO lives in TMEM (the A operand of dP = dO V^T), which
+  // frees the shared memory for the third K stage.
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kTile;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
+  static constexpr uint32_t kOffDS = kOffV + kVStages * kTile;
+  static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
+  static constexpr int kNumBars = 24;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kOffMisc + 16;
+  static constexpr uint32_t kSmemRequest = kBytes + 1024;
+  static_assert(kSmemRequest <= 232448, "shared memory budget");
+};
+
+// TMEM columns: S [0,128) (lane = query row), dP [128,256), dQ [256,256+D),
+// dO [384, 384+D/2) as bf16 pairs.
 // MMA order per key block j:  S(j+1), [dQ(j) | dP(j+1)]
 // ([a | b]: the MMAs of two products with different accumulators issued
 // alternately) so the rows form P(j+1) while dQ(j) and dP(j+1) run and
-// dS(j+1) while S(j+2) runs.
+// dS(j+1) while S(j+2) runs.  K(j) is read by S(j) and, last, by dQ(j); the
+// third K stage lets K(j+2) load while dQ(j) still holds K(j).
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdParams p) {
-  using L = BwdLayout<D>;
-  constexpr int S = L::kStages;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  using L = DqLayout<D>;
+  constexpr int SK = L::kKStages, SV = L::kVStages;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDO = 384;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-  uint64_t *qdo_full = bars;
-  uint64_t *kv_full = bars + 1;      // [S]
-  uint64_t *kv_empty = kv_full + S;  // [S]
-  uint64_t *s_full = kv_empty + S;
+  uint64_t *q_full = bars;
+  uint64_t *do_ready = q_full + 1;    // dO written to TMEM by the rows
+  uint64_t *k_full = do_ready + 1;    // [SK]
+  uint64_t *k_empty = k_full + SK;    // [SK]
+  uint64_t *v_full = k_empty + SK;    // [SV]
+  uint64_t *v_empty = v_full + SV;    // [SV]
+  uint64_t *s_full = v_empty + SV;
   uint64_t *dp_full = s_full + 1;
   uint64_t *s_free = dp_full + 1;
   uint64_t *ds_ready = s_free + 1;
   uint64_t *ds_free = ds_ready + 1;
   uint64_t *dq_done = ds_free + 1;
   uint64_t *drain = dq_done + 1;
+  static_assert(2 + 2 * SK + 2 * SV + 7 <= L::kNumBars, "barrier slots");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
   const WaitCtl ctl{abort_flag, p.status};
@@ -511,10 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv = CAUSAL ? (iblk + 1) : nblk;  // key blocks 0 .. n_kv-1
 
   if (threadIdx.x == 0) {
-    mbar_init(qdo_full, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    mbar_init(q_full, 1);
+    mbar_init(do_ready, 128);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -535,58 +572,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t *sQ = smem + L::kOffRes0;
-  uint8_t *sDO = smem + L::kOffRes1;
-  uint8_t *sK = smem + L::kOffRing0;
-  uint8_t *sV = smem + L::kOffRing1;
+  uint8_t *sQ = smem + L::kOffQ;
+  uint8_t *sK = smem + L::kOffK;
+  uint8_t *sV = smem + L::kOffV;
   uint8_t *sDS = smem + L::kOffDS;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
+      // Q once, then the K ring
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(qdo_full, 2 * L::kTile);
+      mbar_arrive_expect_tx(q_full, L::kTile);
 #pragma unroll
-      for (int s = 0; s < L::kSlabs; ++s) {
-        tma_load_3d(sQ + s * kBlk * 128, &tm_q, qdo_full, s * 64, iblk * kBlk, bh);
-        tma_load_3d(sDO + s * kBlk * 128, &tm_do, qdo_full, s * 64, iblk * kBlk, bh);
-      }
+      for (int s = 0; s < L::kSlabs; ++s) tma_load_3d(sQ + s * kBlk * 128, &tm_q, q_full, s * 64, iblk * kBlk, bh);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1, ctl, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTile);
+        const int st = j % SK;
+        if (!mbar_wait(&k_empty[st], ((j / SK) & 1) ^ 1, ctl, kSiteKEmpty)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::kTile);
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s) {
-          tma_load_3d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &kv_full[st], s * 64, j * kBlk, bh);
-          tma_load_3d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &kv_full[st], s * 64, j * kBlk, bh);
-        }
+        for (int s = 0; s < L::kSlabs; ++s)
+          tma_load_3d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, j * kBlk, bh);
         issued = j + 1;
       }
       if (*abort_flag) {
-        mbar_drain(qdo_full, 0);
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_drain(&kv_full[j % S], (j / S) & 1);
+        mbar_drain(q_full, 0);
+        for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
       }
+    } else if (lane == 1) {
+      // the V ring
+      tma_prefetch_desc(&tm_v);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % SV;
+        if (!mbar_wait(&v_empty[st], ((j / SV) & 1) ^ 1, ctl, kSiteVEmpty)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::kTile);
+#pragma unroll
+        for (int s = 0; s < L::kSlabs; ++s)
+          tma_load_3d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, j * kBlk, bh);
+        issued = j + 1;
+      }
+      if (*abort_flag)
+        for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&v_full[j % SV], (j / SV) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kBlk, kBlk, false, false);  // S, dP
       constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, false, true);      // dQ
-      const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO), aK = smem_addr(sK), aV = smem_addr(sV),
-                     aDS = smem_addr(sDS);
-      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ;
+      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV), aDS = smem_addr(sDS);
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ, tDO = tmem + kColDO;
 
       // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
       // a compile-time step offset (all issue loops are unrolled).
-      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dDO = sdesc_sw128(aDO, 16, 1024);
-      const uint64_t dDS = sdesc_sw128(aDS, 16, 1024);
-      auto k_kmaj = [&](int j) { return sdesc_sw128(aK + (j % S) * L::kTile, 16, 1024); };
-      auto k_mn = [&](int j) { return sdesc_sw128(aK + (j % S) * L::kTile, kBlk * 128, 1024); };
-      auto v_kmaj = [&](int j) { return sdesc_sw128(aV + (j % S) * L::kTile, 16, 1024); };
+      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dDS = sdesc_sw128(aDS, 16, 1024);
+      auto k_kmaj = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, 16, 1024); };
+      auto k_mn = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, kBlk * 128, 1024); };
+      auto v_kmaj = [&](int j) { return sdesc_sw128(aV + (j % SV) * L::kTile, 16, 1024); };
 
       // S(j) = Q K_j^T (both K-major over d)
       auto issue_s = [&](int j) {
@@ -596,12 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tS, desc_add(dQ, kmajor_step(kk, kBlk)), desc_add(bk, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
         tc_commit(s_full);
       };
-      // dP(j) = dO V_j^T (K-major over d), alone or interleaved with dQ += dS K
+      // one K step of dP(j) = dO V_j^T (dO from TMEM, V_j K-major over d)
       auto dp_step = [&](uint64_t bv, int kk) {
-        mma_ss(tDP, desc_add(dDO, kmajor_step(kk, kBlk)), desc_add(bv, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
+        mma_ts(tDP, tDO + kk * 8, desc_add(bv, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
       };
 
-      bool ok = mbar_wait(qdo_full, 0, ctl, kSiteQFull) && mbar_wait(&kv_full[0], 0, ctl, kSiteKFull);
+      bool ok = mbar_wait(q_full, 0, ctl, kSiteQFull) && mbar_wait(&k_full[0], 0, ctl, kSiteKFull) &&
+                mbar_wait(&v_full[0], 0, ctl, kSiteVFull) && mbar_wait(do_ready, 0, ctl, kSiteDoFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -609,13 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
         tc_commit(dp_full);
+        tc_commit(&v_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % S;
         const bool more = j + 1 < n_kv;
         if (more) {
           // S(j+1) once the rows have read S(j)
-          if (!(ok = mbar_wait(&kv_full[(j + 1) % S], ((j + 1) / S) & 1, ctl, kSiteKFull))) break;
+          if (!(ok = mbar_wait(&k_full[(j + 1) % SK], ((j + 1) / SK) & 1, ctl, kSiteKFull))) break;
           if (!(ok = mbar_wait(s_free, j & 1, ctl, kSiteSFull))) break;
           tc_fence_after();
           issue_s(j + 1);
@@ -623,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ += dS K_j (dS K-major over keys; K_j MN-major over d) once dS(j)
         // is in smem, interleaved with dP(j+1) (the rows have read dP(j))
         if (!(ok = mbar_wait(ds_ready, j & 1, ctl, kSiteDsReady))) break;
+        if (more && !(ok = mbar_wait(&v_full[(j + 1) % SV], ((j + 1) / SV) & 1, ctl, kSiteVFull))) break;
         tc_fence_after();
         {
           const uint64_t bk = k_mn(j), bv = more ? v_kmaj(j + 1) : 0;
@@ -633,9 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (more && kk < D / 16) dp_step(bv, kk);
           }
         }
-        if (more) tc_commit(dp_full);
+        if (more) {
+          tc_commit(dp_full);
+          tc_commit(&v_empty[(j + 1) % SV]);
+        }
         tc_commit(ds_free);
-        tc_commit(&kv_empty[st]);
+        tc_commit(&k_empty[j % SK]);
       }
       if (ok) tc_commit(dq_done);
       tc_commit(drain);
@@ -656,6 +704,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
     bool ok = true;
 
+    // dO row -> TMEM (bf16 pairs over D/2 columns): the A operand of dP.
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.dout + (static_cast<size_t>(bh) * N + qrow) * D);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = qrow < N ? src[h * 8 + u] : make_uint4(0, 0, 0, 0);
+          v[4 * u] = x.x;
+          v[4 * u + 1] = x.y;
+          v[4 * u + 2] = x.z;
+          v[4 * u + 3] = x.w;
+        }
+        tmem_st32(tmem + kColDO + lane_base + h * 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(do_ready);
+    }
+
     for (int j = 0; j < n_kv; ++j) {
       const bool diag = CAUSAL && (j == iblk);
       // Phase 1: P = exp2(S c - lse2), kept as bf16 pairs.
@@ -666,11 +735,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint32_t pk[64];
+      uint32_t sva[4][32];
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tS + ch * 32, sva[ch]);
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(sva[ch]);
+      tc_fence_before();
+      mbar_arrive(s_free);  // S is in registers: the next S may overwrite it
 #pragma unroll
       for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t sv[32];
-        tmem_ld32(tS + ch * 32, sv);
-        tmem_ld_wait(sv);
+        const uint32_t(&sv)[32] = sva[ch];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
@@ -682,8 +756,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[ch * 16 + e / 2] = pack_bf16x2(p0, p1);
         }
       }
-      tc_fence_before();
-      mbar_arrive(s_free);
 
       // Phase 2: dS = P o (dP - D) -> bf16 into the swizzled [query][key] tile.
       ok = mbar_wait(dp_full, j & 1, ctl, kSiteSFull);
@@ -693,11 +765,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      uint32_t dpa[4][32];
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tDP + ch * 32, dpa[ch]);
+#pragma unroll
+      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(dpa[ch]);
 #pragma unroll
       for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t dpv[32];
-        tmem_ld32(tDP + ch * 32, dpv);
-        tmem_ld_wait(dpv);
+        const uint32_t(&dpv)[32] = dpa[ch];
         uint32_t dsv[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -757,7 +832,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
+  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL>, grid, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
   return cudaSuccess;

@@ -122,27 +122,28 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     }
 
     // Block max of t = s * c (a min of s when the scale is negative).
+    // (one partial per 32-column quarter keeps the dependency chains short)
     float mx;
     if (!neg) {
-      float m0 = -INFINITY, m1 = -INFINITY;
+      float mq[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float m0 = fmax3(__uint_as_float(s[q4][0]), __uint_as_float(s[q4][1]), __uint_as_float(s[q4][2]));
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          m0 = fmax3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
-          m1 = fmax3(m1, __uint_as_float(s[q4][i + 2]), __uint_as_float(s[q4][i + 3]));
-        }
-      mx = fmaxf(m0, m1);
+        for (int i = 3; i < 31; i += 2) m0 = fmax3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
+        mq[q4] = fmaxf(m0, __uint_as_float(s[q4][31]));
+      }
+      mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
     } else {
-      float m0 = INFINITY, m1 = INFINITY;
+      float mq[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float m0 = fmin3(__uint_as_float(s[q4][0]), __uint_as_float(s[q4][1]), __uint_as_float(s[q4][2]));
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          m0 = fmin3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
-          m1 = fmin3(m1, __uint_as_float(s[q4][i + 2]), __uint_as_float(s[q4][i + 3]));
-        }
-      mx = fminf(m0, m1);
+        for (int i = 3; i < 31; i += 2) m0 = fmin3(m0, __uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1]));
+        mq[q4] = fminf(m0, __uint_as_float(s[q4][31]));
+      }
+      mx = fminf(fminf(mq[0], mq[1]), fminf(mq[2], mq[3]));
     }
     const float m_cand = mx * c;
     const bool grow = m_cand > m_run + kRescaleThreshold;
@@ -163,6 +164,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t pk[16];
+      float2 sfq = make_float2(0.f, 0.f), sbq = make_float2(0.f, 0.f);  // per-quarter partial sums
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const float2 x = ffma2(make_float2(__uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1])), cc, nm);
@@ -173,10 +175,12 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
         }
         const uint32_t b = pack_bf16x2(p0, p1);
         pk[i / 2] = b;
-        sf = fadd2(sf, make_float2(p0, p1));
-        sb = fadd2(sb, make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
+        sfq = fadd2(sfq, make_float2(p0, p1));
+        sbq = fadd2(sbq, make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
       }
       tmem_st16(tS + q4 * 16, pk);
+      sf = fadd2(sf, sfq);
+      sb = fadd2(sb, sbq);
     }
     const float sum0 = sf.x, sum1 = sf.y;
     lb_run += sb.x + sb.y;
