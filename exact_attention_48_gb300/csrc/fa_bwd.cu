@@ -24,8 +24,9 @@
 // bounds the backward pass.
 //
 // Both main kernels: warp 0 TMA producer, warp 1 MMA issuer (one thread),
-// warp 2 TMEM owner, warps 4..7 one row per thread (key row in dK/dV, query
-// row in dQ), working in two phases per block: P from the scores, then dS
+// warp 2 TMEM owner; warps 4..11 own one row each (key row in dK/dV, query
+// row in dQ), two warps per row, each taking one half of the row's 128
+// columns; they work in two phases per block: P from the scores, then dS
 // from dP.
 
 #include "fa_internal.h"
@@ -38,7 +39,12 @@ namespace {
 constexpr int kBlk = 128;  // rows per block, keys and queries alike
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 256;
+// Warps 0..3 are the control warpgroup (producer, MMA issuer, TMEM owner),
+// warps 4..11 the row warps: two warpgroups that split each 128-wide row of
+// scores between them (columns [0,64) and [64,128)), so that every SM
+// sub-partition runs two row warps and one can issue while the other waits.
+constexpr int kThreads = 384;
+constexpr int kRowThreads = 256;
 
 // ------------------------------------------------------------------ pre
 
@@ -145,8 +151,9 @@ struct BwdLayout {
 
 // ------------------------------------------------------------------ dK, dV
 
-// TMEM columns: S^T [0,128) (P^T as bf16 pairs over its first 64 columns),
-// dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The products are
+// TMEM columns: S^T [0,128) (P^T of queries [64h, 64h+64) as bf16 pairs
+// over columns [64h, 64h+32), h = 0, 1: each half writes over scores it has
+// already read), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The products are
 // formed transposed (S^T = K Q^T, dP^T = V dO^T) so the key row, which owns
 // dK and dV, is the TMEM lane.  MMA order per query block t:
 //   dV(t), S^T(t+1), [dK(t) | dP^T(t+1)]
@@ -205,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 128);
-    mbar_init(ds_ready, 128);
+    mbar_init(p_ready, kRowThreads);
+    mbar_init(ds_ready, kRowThreads);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -311,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint64_t bdo = do_mn(t);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tDV, tS + kk * 8, desc_add(bdo, mnmajor_step(kk)), kIdescKV, (t > 0 || kk > 0));
+          for (int kk = 0; kk < kBlk / 16; ++kk)  // P^T of queries [64h, 64h+64) sits at columns 64h..
+            mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bdo, mnmajor_step(kk)), kIdescKV,
+                   (t > 0 || kk > 0));
         }
         // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
         // first, reads P^T(t) before S^T(t+1) overwrites it
@@ -344,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ key rows
+    const int half = (warp >> 2) - 1;  // query columns [64 half, 64 half + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the block
     const int key = jblk * kBlk + r;
@@ -355,35 +364,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *delta_h = p.delta + static_cast<size_t>(bh) * Np;
     const uint32_t ds_tile = smem_addr(sDS);
     const bool key_ok = key < N;
+    const int c0 = half * 64;  // first query column of this half
     bool ok = true;
+    if (half == 0 && wq == 0 && lane < 8) prefetch_l1((lane < 4 ? lse2_h : delta_h) + i0 * kBlk + (lane & 3) * 32);
 
     for (int t = 0; t < n_q; ++t) {
       const int i = i0 + t;
       // per-query statistics of this block (same for every thread: L1 broadcasts)
-      const float4 *lse4 = reinterpret_cast<const float4 *>(lse2_h + i * kBlk);
-      const float4 *del4 = reinterpret_cast<const float4 *>(delta_h + i * kBlk);
+      const float4 *lse4 = reinterpret_cast<const float4 *>(lse2_h + i * kBlk + c0);
+      const float4 *del4 = reinterpret_cast<const float4 *>(delta_h + i * kBlk + c0);
       const bool diag = CAUSAL && (i == jblk);
+      // the next block's statistics into L1 now (8 lines of 128 bytes)
+      if (t + 1 < n_q && half == 0 && wq == 0 && lane < 8)
+        prefetch_l1((lane < 4 ? lse2_h : delta_h) + (i + 1) * kBlk + (lane & 3) * 32);
 
-      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [0, 64).
+      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + 32).
       ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t pk[64];  // P^T row, bf16 pairs, kept for phase 2
-      uint32_t sva[4][32];
+      uint32_t pk[32];  // P^T of this half row, bf16 pairs, kept for phase 2
+      uint32_t sva[2][32];
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tS + ch * 32, sva[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(sva[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&sv)[32] = sva[ch];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const int qc = ch * 32 + e;  // query column within the block
-          const float4 l4 = __ldg(lse4 + qc / 4);
+          const int qh = ch * 32 + e;  // query column within the half
+          const float4 l4 = __ldg(lse4 + qh / 4);
           const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), make_float2(c, c),
                                    make_float2(-l4.x, -l4.y));
           const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
@@ -391,18 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            if (diag) pr[u] = (qc + u >= r) ? pr[u] : 0.0f;  // key r visible to query qc+u iff r <= qc+u
+            if (diag) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
             if (!key_ok) pr[u] = 0.0f;
           }
-          pk[qc / 2] = pack_bf16x2(pr[0], pr[1]);
-          pk[qc / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+          pk[qh / 2] = pack_bf16x2(pr[0], pr[1]);
+          pk[qh / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
         }
-        // columns [16 ch, 16 ch + 16) of S^T hold queries already read
-        uint32_t part[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) part[u] = pk[ch * 16 + u];
-        tmem_st16(tS + ch * 16, part);
       }
+      tmem_st32(tS + c0, pk);  // over scores of this half, already read
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -414,20 +424,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t dpa[4][32];
+      uint32_t dpa[2][32];
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tDP + ch * 32, dpa[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(dpa[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&dpv)[32] = dpa[ch];
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const int qc = ch * 32 + e;
-          const float4 d4 = __ldg(del4 + qc / 4);
-          const uint32_t p01 = pk[qc / 2], p23 = pk[qc / 2 + 1];
+          const int qh = ch * 32 + e;
+          const float4 d4 = __ldg(del4 + qh / 4);
+          const uint32_t p01 = pk[qh / 2], p23 = pk[qh / 2 + 1];
           const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
                                    make_float2(-d4.x, -d4.y));
           const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
@@ -439,13 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
           dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
         }
-        store_row_sw128(ds_tile, r, ch * 32, dk);
+        store_row_sw128(ds_tile, r, c0 + ch * 32, dk);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
-    // dV and dK epilogues (the scale of dK applied here)
+    // epilogues: the first half writes dV, the second dK (scale applied here)
     if (ok) {
       ok = mbar_wait(acc_done, 0, ctl, kSiteMmaDone);
       ok = __all_sync(0xffffffffu, ok);
@@ -453,8 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t row = static_cast<size_t>(bh) * N + key;
-      store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row * D, key_ok, 1.0f);
-      store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row * D, key_ok, p.scale);
+      if (half == 0)
+        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row * D, key_ok, 1.0f);
+      else
+        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row * D, key_ok, p.scale);
     }
   }
 
@@ -544,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(do_ready, 128);
+    mbar_init(do_ready, kRowThreads);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -555,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(ds_ready, 128);
+    mbar_init(s_free, kRowThreads);
+    mbar_init(ds_ready, kRowThreads);
     mbar_init(ds_free, 1);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
@@ -691,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ query rows
+    const int half = (warp >> 2) - 1;  // key columns [64 half, 64 half + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // query row within the block
     const int qrow = iblk * kBlk + r;
@@ -702,23 +715,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float dlt = p.delta[srow];
     const uint32_t ds_tile = smem_addr(sDS);
     const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
+    const int c0 = half * 64;  // first key column of this half
     bool ok = true;
 
     // dO row -> TMEM (bf16 pairs over D/2 columns): the A operand of dP.
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(p.dout + (static_cast<size_t>(bh) * N + qrow) * D);
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
+      for (int hh = 0; hh < D / 64; ++hh) {
+        if ((hh & 1) != half) continue;  // the two halves share the 64-element pieces
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = qrow < N ? src[h * 8 + u] : make_uint4(0, 0, 0, 0);
+          const uint4 x = qrow < N ? src[hh * 8 + u] : make_uint4(0, 0, 0, 0);
           v[4 * u] = x.x;
           v[4 * u + 1] = x.y;
           v[4 * u + 2] = x.z;
           v[4 * u + 3] = x.w;
         }
-        tmem_st32(tmem + kColDO + lane_base + h * 32, v);
+        tmem_st32(tmem + kColDO + lane_base + hh * 32, v);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -727,31 +742,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < n_kv; ++j) {
       const bool diag = CAUSAL && (j == iblk);
-      // Phase 1: P = exp2(S c - lse2), kept as bf16 pairs.
+      // Phase 1: P = exp2(S c - lse2) for this half of the keys, kept as bf16 pairs.
       ok = mbar_wait(s_full, j & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t pk[64];
-      uint32_t sva[4][32];
+      uint32_t pk[32];
+      uint32_t sva[2][32];
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tS + ch * 32, sva[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(sva[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
       tc_fence_before();
       mbar_arrive(s_free);  // S is in registers: the next S may overwrite it
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&sv)[32] = sva[ch];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
           float p0 = ex2(x.x), p1 = ex2(x.y);
           if (diag) {  // key kc visible to query r iff kc <= r
-            p0 = (ch * 32 + e <= r) ? p0 : 0.0f;
-            p1 = (ch * 32 + e + 1 <= r) ? p1 : 0.0f;
+            p0 = (c0 + ch * 32 + e <= r) ? p0 : 0.0f;
+            p1 = (c0 + ch * 32 + e + 1 <= r) ? p1 : 0.0f;
           }
           pk[ch * 16 + e / 2] = pack_bf16x2(p0, p1);
         }
@@ -765,13 +780,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t dpa[4][32];
+      uint32_t dpa[2][32];
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld32(tDP + ch * 32, dpa[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) tmem_ld_wait(dpa[ch]);
+      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&dpv)[32] = dpa[ch];
         uint32_t dsv[16];
 #pragma unroll
@@ -782,21 +797,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               ffma2(make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)), g, make_float2(0.f, 0.f));
           dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
-        store_row_sw128(ds_tile, r, ch * 32, dsv);
+        store_row_sw128(ds_tile, r, c0 + ch * 32, dsv);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
-    // dQ epilogue (the scale applied here)
+    // dQ epilogue (the scale applied here): each half writes D/2 columns
     if (ok) {
       ok = mbar_wait(dq_done, 0, ctl, kSiteMmaDone);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      store_acc_row<D>(tmem + kColDQ + lane_base, p.dq + (static_cast<size_t>(bh) * N + qrow) * D, qrow < N,
-                       p.scale);
+      store_acc_row<D / 2>(tmem + kColDQ + lane_base + half * (D / 2),
+                           p.dq + (static_cast<size_t>(bh) * N + qrow) * D + half * (D / 2), qrow < N, p.scale);
     }
   }
 
