@@ -44,7 +44,7 @@ constexpr uint32_t kTmemCols = 512;
 // scores between them (columns [0,64) and [64,128)), so that every SM
 // sub-partition runs two row warps and one can issue while the other waits.
 constexpr int kThreads = 384;
-constexpr int kRowThreads = 256;
+constexpr int kRowWarps = 8;  // row warps; each signals its barriers once (lane 0)
 
 // ------------------------------------------------------------------ pre
 
@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, kRowThreads);
-    mbar_init(ds_ready, kRowThreads);
+    mbar_init(p_ready, kRowWarps);
+    mbar_init(ds_ready, kRowWarps);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tS + c0, pk);  // over scores of this half, already read
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      warp_arrive(p_ready);
 
       // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 into the swizzled dS^T tile.
       ok = mbar_wait(dp_full, t & 1, ctl, kSiteSFull);
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      warp_arrive(ds_ready);
     }
     // epilogues: the first half writes dV, the second dK (scale applied here)
     if (ok) {
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(do_ready, kRowThreads);
+    mbar_init(do_ready, kRowWarps);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -567,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(s_free, kRowThreads);
-    mbar_init(ds_ready, kRowThreads);
+    mbar_init(s_free, kRowWarps);
+    mbar_init(ds_ready, kRowWarps);
     mbar_init(ds_free, 1);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(do_ready);
+      warp_arrive(do_ready);
     }
 
     for (int j = 0; j < n_kv; ++j) {
@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
       tc_fence_before();
-      mbar_arrive(s_free);  // S is in registers: the next S may overwrite it
+      warp_arrive(s_free);  // S is in registers: the next S may overwrite it
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&sv)[32] = sva[ch];
@@ -801,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      warp_arrive(ds_ready);
     }
     // dQ epilogue (the scale applied here): each half writes D/2 columns
     if (ok) {

@@ -152,19 +152,18 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
       alpha = ex2(m_run - m_cand);
       m_run = m_cand;
     }
-    l_run *= alpha;
-    lb_run *= alpha;
     const float2 cc = make_float2(c, c), nm = make_float2(-m_run, -m_run);
 
-    // P = exp2(t - m) as bf16 pairs over the first 64 columns of S, one
-    // quarter (32 keys -> 16 columns) at a time to keep few values live.
-    // Two row sums: of the fp32 P (for the logsumexp) and of the bf16 P the
-    // P V product uses (for O, so the weights applied to V add up to one).
-    float2 sf = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+    // P = exp2(t - m) as bf16 pairs over the first 64 columns of S (the A
+    // operand of the P V product), one quarter (32 keys -> 16 columns) at a
+    // time.  The sum of the fp32 P (for the logsumexp) is taken on the way;
+    // the sum of the bf16 P (for O) waits until the MMA warp has been
+    // released (below), off the path that the tensor core waits on.
+    uint32_t pk[4][16];
+    float2 sf = make_float2(0.f, 0.f);
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t pk[16];
-      float2 sfq = make_float2(0.f, 0.f), sbq = make_float2(0.f, 0.f);  // per-quarter partial sums
+      float2 sfq = make_float2(0.f, 0.f);  // per-quarter partial sum
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const float2 x = ffma2(make_float2(__uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1])), cc, nm);
@@ -173,44 +172,54 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
           p0 = (q4 * 32 + i <= lim) ? p0 : 0.0f;
           p1 = (q4 * 32 + i + 1 <= lim) ? p1 : 0.0f;
         }
-        const uint32_t b = pack_bf16x2(p0, p1);
-        pk[i / 2] = b;
+        pk[q4][i / 2] = pack_bf16x2(p0, p1);
         sfq = fadd2(sfq, make_float2(p0, p1));
-        sbq = fadd2(sbq, make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
       }
-      tmem_st16(tS + q4 * 16, pk);
+      tmem_st16(tS + q4 * 16, pk[q4]);
       sf = fadd2(sf, sfq);
-      sb = fadd2(sb, sbq);
     }
-    const float sum0 = sf.x, sum1 = sf.y;
-    lb_run += sb.x + sb.y;
-    l_run += sum0 + sum1;
     tmem_st_wait();
 
-    // O of the previous block must be complete before it is rescaled and
-    // before the next product accumulates into it.
-    if (j > 0) {
+    // A row whose max moved rescales O, which needs the previous product
+    // complete (it is: S of this block was issued after it, and S is
+    // complete; the wait only makes that explicit).  Rows that keep their
+    // max leave O alone, and the next product simply accumulates into it.
+    if (j > 0 && __any_sync(0xffffffffu, grow)) {
       ok = mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      if (__any_sync(0xffffffffu, grow)) {
+      {
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
-          tmem_ld_wait(o);
+        for (int ch = 0; ch < D / 16; ++ch) {  // 16 columns at a time: P stays in registers meanwhile
+          uint32_t o[16];
+          tmem_ld16(tO + ch * 16, o);
+          tmem_ld_wait16(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + ch * 32, o);
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(tO + ch * 16, o);
         }
         tmem_st_wait();
       }
     }
     tc_fence_before();
-    mbar_arrive(a.p_ready);
+    warp_arrive(a.p_ready);
+
+    // Sum of the bf16 P the P V product used: O is divided by it, so that
+    // the weights applied to V add up to one.
+    float2 sb = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float2 sbq = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        sbq = fadd2(sbq, make_float2(__uint_as_float(pk[q4][i] << 16), __uint_as_float(pk[q4][i] & 0xFFFF0000u)));
+      sb = fadd2(sb, sbq);
+    }
+    l_run = l_run * alpha + (sf.x + sf.y);
+    lb_run = lb_run * alpha + (sb.x + sb.y);
   }
 
   // Epilogue: O / l in bf16 and the natural-log logsumexp.
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_ready[t], 128);
+      mbar_init(&p_ready[t], 4);  // one arrival per softmax warp of the tile
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
