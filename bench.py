@@ -37,12 +37,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--causal", action="store_true", help="time the causal variant of the workload")
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--workload", choices=["sweep", "fwd_b8h16n2048d64", "causal_b4h32n4096d128",
+                                           "long_b1h16n16384d128x2"], default="sweep",
+                    help="a named workload instead of the sweep point given by --N/--d/--causal "
+                         "(the forward-only one times the forward alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true",
@@ -51,8 +55,12 @@ def parse_args():
 
 
 def workload(args):
-    from exact_attention_48_gb300.inputs import sweep
-    return sweep(args.N, args.d, args.causal)
+    from exact_attention_48_gb300 import inputs
+    named = {"fwd_b8h16n2048d64": inputs.FWD_B8H16N2048D64, "causal_b4h32n4096d128": inputs.CAUSAL_B4H32N4096D128,
+             "long_b1h16n16384d128x2": inputs.LONG_B1H16N16384D128}
+    if getattr(args, "workload", "sweep") != "sweep":
+        return named[args.workload]
+    return inputs.sweep(args.N, args.d, args.causal)
 
 
 def dist_setup():
@@ -218,17 +226,32 @@ def aggregate_throughput(flops_per_step_per_rank: float, steps: int, local_ms: f
 
 # ------------------------------------------------------------------ GPU
 
+def touched_bytes(w):
+    n_t = 8 if w.backward else 4  # q, k, v, o (+ dO, dQ, dK, dV)
+    return n_t * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.N * 4
+
+
+def needs_flush(w):
+    return touched_bytes(w) < 2 * L2_BYTES
+
+
 def config_of(w):
-    return {"workload": f"fwd+bwd B{w.B} H{w.H} N{w.N} d{w.d} {'causal' if w.causal else 'non-causal'} bf16",
+    touched = touched_bytes(w)
+    l2 = (f"no flush: the tensors touched per step ({touched / 2**20:.0f} MiB) are larger than the 129 MB L2"
+          if not needs_flush(w) else
+          f"L2 flushed between steps (a 256 MiB write); the tensors touched per step ({touched / 2**20:.0f} MiB) "
+          f"would fit in L2; value = work / sum of the per-step CUDA-event times")
+    return {"workload": f"{'fwd+bwd' if w.backward else 'fwd'} B{w.B} H{w.H} N{w.N} d{w.d} "
+                        f"{'causal' if w.causal else 'non-causal'} bf16",
             "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
             "inputs": f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}",
-            "l2": "no flush: the tensors touched per step (q,k,v,o,dO,dq,dk,dv + fp32 dQ accumulator) "
-                  "are several times larger than the 129 MB L2"}
+            "l2": l2}
 
 
-def traffic_record(kernel: str):
+def traffic_record(kernel: str, workload_name: str):
     """DRAM bytes per launch from the committed ncu summary, or None if the
-    kernel source changed since those counters were taken."""
+    kernel source changed since those counters were taken or they were taken
+    on another workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -244,7 +267,7 @@ def traffic_record(kernel: str):
         return None
     if h != rec.get("source_sha256_16"):
         return None
-    if rec.get("workload") != rec.get("bench_workload"):
+    if rec.get("workload") != workload_name:
         return None
     return float(rec["bytes_per_launch"])
 
@@ -272,14 +295,18 @@ def run_ours(args):
     ws = torch.empty(fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
+    bwd_on = w.backward  # the forward-only workload times the forward alone
+
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
         fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
         if evs is not None:
             evs[1].record(stream)
-            fa_debug_time_next_bwd(evs[2], evs[3], evs[4])
-        fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if bwd_on:
+            if evs is not None:
+                fa_debug_time_next_bwd(evs[2], evs[3], evs[4])
+            fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         if evs is not None:
             evs[5].record(stream)
 
@@ -302,8 +329,11 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    flush = torch.empty(256 * 2**20, device="cuda", dtype=torch.uint8) if needs_flush(w) else None
     start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
         step(evs[i])
     stop.record(stream)
     torch.cuda.synchronize()
@@ -313,27 +343,32 @@ def run_ours(args):
     if fa_device_status() != 0:
         raise SystemExit("device status error in the timed region")
 
-    flops_step = w.flops_fwd() + w.flops_bwd()
-    value, elapsed_ms = aggregate_throughput(flops_step, args.steps, start.elapsed_time(stop), world, "cuda")
+    flops_step = w.flops_fwd() + (w.flops_bwd() if bwd_on else 0.0)
+    total_ms = start.elapsed_time(stop)
+    if flush is not None:  # leave the flushes out: the steps' own event times
+        total_ms = sum(e[0].elapsed_time(e[5]) for e in evs)
+    value, elapsed_ms = aggregate_throughput(flops_step, args.steps, total_ms, world, "cuda")
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
-    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    if bwd_on:
+        bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
+        dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
     fwd_tf = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12
+    bwd_tf = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12 if bwd_on else None
     # Per-kernel tensor work actually executed (the dense products of each
     # kernel, in units of the forward's 4*B*H*N^2*d): forward 1.0, dK/dV 2.0
     # (S^T, dP^T, dV, dK), dQ 1.5 (S, dP, dQ).  The backward headline keeps
     # the 2.5x count of the metric and credits no recomputation.
-    kernels = [("fa_fwd_kernel", fwd_ms, 1.0 * w.flops_fwd()),
-               ("fa_bwd_dkdv_kernel", dkdv_ms, 2.0 * w.flops_fwd()),
-               ("fa_bwd_dq_kernel", dq_ms, 1.5 * w.flops_fwd())]
+    kernels = [("fa_fwd_kernel", fwd_ms, 1.0 * w.flops_fwd())]
+    if bwd_on:
+        kernels += [("fa_bwd_dkdv_kernel", dkdv_ms, 2.0 * w.flops_fwd()),
+                    ("fa_bwd_dq_kernel", dq_ms, 1.5 * w.flops_fwd())]
     dom, dom_ms, dom_flops = max(kernels, key=lambda k: k[1])
     dom_tf = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = traffic_record(dom)
+    traffic = traffic_record(dom, config_of(w)["workload"])
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -342,15 +377,15 @@ def run_ours(args):
         "config": config_of(w),
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_sustained": fwd_tf / peak_sus,
                 "frac_of_burst": fwd_tf / peak_burst},
-        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_sustained": bwd_tf / peak_sus,
-                "frac_of_burst": bwd_tf / peak_burst},
+        "bwd": ({"ms": bwd_ms, "tflops": bwd_tf, "frac_of_sustained": bwd_tf / peak_sus,
+                 "frac_of_burst": bwd_tf / peak_burst} if bwd_on else None),
         "kernels": {name: {"ms": ms, "tensor_tflops_executed": fl / (ms * 1e-3) / 1e12,
                            "frac_of_sustained": fl / (ms * 1e-3) / 1e12 / peak_sus} for name, ms, fl in kernels},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": dom_tf,
                      "peak": peak_sus, "unit": "TFLOP/s", "frac": dom_tf / peak_sus,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                      "flops_per_launch": dom_flops, "traffic": traffic},
-        "gpu_launches": 4 * args.steps,  # fwd; bwd pre, dK/dV, dQ
+        "gpu_launches": (4 if bwd_on else 1) * args.steps,  # fwd; bwd pre, dK/dV, dQ
         "clocks": clk,
     }
 
@@ -379,13 +414,15 @@ def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
     lse_ = torch.empty((w.B, w.H, w.N), device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 20))
+    n_in, n_out = (4, 4) if w.backward else (3, 1)
 
     def step():
-        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo))[:n_in]:
             dst.copy_(src, non_blocking=True)
         fa_fwd(q_, k_, v_, w.causal, w.scale, o=o_, lse=lse_)
-        fa_bwd(q_, k_, v_, o_, do_, lse_, w.causal, w.scale, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
-        for dst, src in zip(outs, (o_, dq_, dk_, dv_)):
+        if w.backward:
+            fa_bwd(q_, k_, v_, o_, do_, lse_, w.causal, w.scale, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
+        for dst, src in zip(outs, (o_, dq_, dk_, dv_)[:n_out]):
             dst.copy_(src, non_blocking=True)
         hlse.copy_(lse_, non_blocking=True)
 
@@ -398,11 +435,11 @@ def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    flops = w.flops_fwd() + w.flops_bwd()
+    flops = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
     value, ms = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
     nbytes = q.numel() * q.element_size()
     return {"value": value, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes + hlse.numel() * 4,
+            "h2d_bytes_per_step": n_in * nbytes, "d2h_bytes_per_step": n_out * nbytes + hlse.numel() * 4,
             "steps": steps}
 
 
