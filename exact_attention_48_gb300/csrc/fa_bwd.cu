@@ -385,7 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t pk[32];  // P^T of this half row, bf16 pairs, kept for phase 2
+      // P^T of this half row in fp32 pairs (kept for phase 2) and as bf16
+      // pairs in TMEM.  Key rows past N (zero rows of K, so S = 0) get a
+      // finite P that only reaches their own dV, dK rows, which are not
+      // stored: no mask needed.
+      float2 pf[32];
       uint32_t sva[2][32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
@@ -394,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const uint32_t(&sv)[32] = sva[ch];
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int qh = ch * 32 + e;  // query column within the half
@@ -403,16 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
                                    make_float2(c, c), make_float2(-l4.z, -l4.w));
           float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+          if (diag) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (diag) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
-            if (!key_ok) pr[u] = 0.0f;
+            for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
           }
-          pk[qh / 2] = pack_bf16x2(pr[0], pr[1]);
-          pk[qh / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+          pf[qh / 2] = make_float2(pr[0], pr[1]);
+          pf[qh / 2 + 1] = make_float2(pr[2], pr[3]);
+          pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
+          pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
         }
+        tmem_st16(tS + c0 + ch * 16, pk);  // over scores of this half, already read
       }
-      tmem_st32(tS + c0, pk);  // over scores of this half, already read
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(p_ready);
@@ -437,15 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 4) {
           const int qh = ch * 32 + e;
           const float4 d4 = __ldg(del4 + qh / 4);
-          const uint32_t p01 = pk[qh / 2], p23 = pk[qh / 2 + 1];
           const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
                                    make_float2(-d4.x, -d4.y));
           const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
                                    make_float2(-d4.z, -d4.w));
-          const float2 ds01 = ffma2(make_float2(__uint_as_float(p01 << 16), __uint_as_float(p01 & 0xFFFF0000u)), g01,
-                                    make_float2(0.f, 0.f));
-          const float2 ds23 = ffma2(make_float2(__uint_as_float(p23 << 16), __uint_as_float(p23 & 0xFFFF0000u)), g23,
-                                    make_float2(0.f, 0.f));
+          const float2 ds01 = fmul2(pf[qh / 2], g01);
+          const float2 ds23 = fmul2(pf[qh / 2 + 1], g23);
           dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
           dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
         }
@@ -749,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t pk[32];
+      float2 pf[32];  // P of this half row (fp32 pairs), kept for phase 2
       uint32_t sva[2][32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
@@ -768,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = (c0 + ch * 32 + e <= r) ? p0 : 0.0f;
             p1 = (c0 + ch * 32 + e + 1 <= r) ? p1 : 0.0f;
           }
-          pk[ch * 16 + e / 2] = pack_bf16x2(p0, p1);
+          pf[ch * 16 + e / 2] = make_float2(p0, p1);
         }
       }
 
@@ -791,10 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t dsv[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const uint32_t pp = pk[ch * 16 + e / 2];
           const float2 g = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd);
-          const float2 ds =
-              ffma2(make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)), g, make_float2(0.f, 0.f));
+          const float2 ds = fmul2(pf[ch * 16 + e / 2], g);
           dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
         store_row_sw128(ds_tile, r, c0 + ch * 32, dsv);

@@ -215,7 +215,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
       float2 sbq = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        sbq = fadd2(sbq, make_float2(__uint_as_float(pk[q4][i] << 16), __uint_as_float(pk[q4][i] & 0xFFFF0000u)));
+        sbq = add_bf16x2_f32(sbq, pk[q4][i]);
       sb = fadd2(sb, sbq);
     }
     l_run = l_run * alpha + (sf.x + sf.y);

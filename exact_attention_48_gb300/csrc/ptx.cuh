@@ -48,6 +48,16 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -137,6 +147,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
       }
     }
   }
+}
+
+// acc.x += the low bf16 of b, acc.y += the high bf16 of b: mixed-precision
+// adds (sm_100+), the bf16 -> f32 widening is exact and each add rounds once.
+__device__ __forceinline__ float2 add_bf16x2_f32(float2 acc, uint32_t b) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(b));
+  return acc;
 }
 
 // Same, without consulting the abort flag: used on the way out to drain
