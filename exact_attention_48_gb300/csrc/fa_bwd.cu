@@ -88,26 +88,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
 
 // ------------------------------------------------------------------ shared pieces
 
-// Byte offset of element (row, col) in a 128-byte-swizzled tile made of
-// 64-column slabs of `rows` rows (the layout the TMA loads produce).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
-  return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
-                               (col & 7) * 2);
-}
-
-// 32 bf16 values (16 pairs) of row r of a [128 x 128] bf16 tile, starting at
-// column col0, into shared memory with the 128-byte swizzle, 16 bytes at a
-// time.
-__device__ __forceinline__ void store_row_sw128(uint32_t tile, int r, int col0, const uint32_t (&v)[16]) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const uint32_t addr = tile + sw128_offset(r, col0 + u * 8, kBlk);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * u]), "r"(v[4 * u + 1]),
-                 "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
-                 : "memory");
-  }
-}
-
 // One row of a TMEM accumulator (lane = row, D fp32 columns), times `mul`,
 // into a bf16 row of global memory.
 template <int D>
@@ -140,8 +120,7 @@ struct BwdLayout {
   static constexpr uint32_t kOffRes1 = kOffRes0 + kTile;
   static constexpr uint32_t kOffRing0 = kOffRes1 + kTile;             // kStages tiles
   static constexpr uint32_t kOffRing1 = kOffRing0 + kStages * kTile;  // kStages tiles
-  static constexpr uint32_t kOffDS = kOffRing1 + kStages * kTile;
-  static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
+  static constexpr uint32_t kOffBar = kOffRing1 + kStages * kTile;
   static constexpr int kNumBars = 16;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffMisc + 16;
@@ -153,13 +132,16 @@ struct BwdLayout {
 
 // TMEM columns: S^T [0,128) (P^T of queries [64h, 64h+64) as bf16 pairs
 // over columns [64h, 64h+32), h = 0, 1: each half writes over scores it has
-// already read), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The products are
-// formed transposed (S^T = K Q^T, dP^T = V dO^T) so the key row, which owns
-// dK and dV, is the TMEM lane.  MMA order per query block t:
-//   dV(t), S^T(t+1), [dK(t) | dP^T(t+1)]
-// ([a | b]: the MMAs of two products with different accumulators issued
-// alternately) so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and
-// dS^T(t+1) while dV(t+1) and S^T(t+2) run.
+// already read), dP^T [128,256) (dS^T the same way over columns
+// [128+64h, 128+64h+32)), dV [256,256+D), dK [256+D,256+2D).  The products
+// are formed transposed (S^T = K Q^T, dP^T = V dO^T) so the key row, which
+// owns dK and dV, is the TMEM lane; P^T and dS^T are then the TMEM A
+// operands of dV += P^T dO and dK += dS^T Q, and never touch shared memory.
+// MMA order per query block t:
+//   dV(t), S^T(t+1), dK(t), dP^T(t+1)
+// so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
+// dV(t+1) and S^T(t+2) run.  Each product that overwrites a TMEM region
+// comes after the one that reads it (the tensor core runs them in order).
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -232,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sV = smem + L::kOffRes1;
   uint8_t *sQ = smem + L::kOffRing0;
   uint8_t *sDO = smem + L::kOffRing1;
-  uint8_t *sDS = smem + L::kOffDS;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -270,30 +251,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescSq = idesc_bf16(kBlk, kBlk, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKV = idesc_bf16(kBlk, D, false, true);      // dV (TMEM A), dK
-      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aDO = smem_addr(sDO),
-                     aDS = smem_addr(sDS);
+      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aDO = smem_addr(sDO);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDV = tmem + kColDV, tDK = tmem + kColDK;
 
       // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
       // a compile-time step offset (all issue loops are unrolled).
       const uint64_t dK = sdesc_sw128(aK, 16, 1024), dV = sdesc_sw128(aV, 16, 1024);
-      const uint64_t dDS = sdesc_sw128(aDS, 16, 1024);
       auto q_kmaj = [&](int t) { return sdesc_sw128(aQ + (t % S) * L::kTile, 16, 1024); };
       auto q_mn = [&](int t) { return sdesc_sw128(aQ + (t % S) * L::kTile, kBlk * 128, 1024); };
       auto do_kmaj = [&](int t) { return sdesc_sw128(aDO + (t % S) * L::kTile, 16, 1024); };
       auto do_mn = [&](int t) { return sdesc_sw128(aDO + (t % S) * L::kTile, kBlk * 128, 1024); };
 
-      // S^T(t) = K Q_t^T and dP^T(t) = V dO_t^T (all operands K-major over
-      // d), interleaved: two independent accumulators keep the tensor pipe
-      // full where one dependent chain runs at about half rate.
-      auto issue_s_dp = [&](int t) {
-        const uint64_t bq = q_kmaj(t), bdo = do_kmaj(t);
+      // S^T(t) = K Q_t^T and dP^T(t) = V dO_t^T (all operands K-major over d)
+      auto issue_dp = [&](int t) {
+        const uint64_t bdo = do_kmaj(t);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss(tS, desc_add(dK, kmajor_step(kk, kBlk)), desc_add(bq, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tDP, desc_add(dV, kmajor_step(kk, kBlk)), desc_add(bdo, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
-        }
-        tc_commit(s_full);
         tc_commit(dp_full);
       };
       auto issue_s = [&](int t) {
@@ -307,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull) && mbar_wait(&qdo_full[0], 0, ctl, kSiteDoFull);
       if (ok) {
         tc_fence_after();
-        issue_s_dp(0);
+        issue_s(0);
+        issue_dp(0);
       }
       for (int t = 0; ok && t < n_q; ++t) {
         const int st = t % S;
@@ -329,22 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(t + 1);
         }
-        // dK += dS^T Q_t (dS^T K-major over queries; Q_t MN-major over d),
-        // interleaved with dP^T(t+1) once the rows have read dP^T(t)
+        // dK += dS^T Q_t (dS^T from TMEM over the dP^T columns; Q_t MN-major
+        // over d), then dP^T(t+1) over them once dK(t) has read them
         if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
         tc_fence_after();
         {
-          const uint64_t bq = q_mn(t), bdo = more ? do_kmaj(t + 1) : 0;
+          const uint64_t bq = q_mn(t);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk) {
-            mma_ss(tDK, desc_add(dDS, kmajor_step(kk, kBlk)), desc_add(bq, mnmajor_step(kk)), kIdescKV,
+          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS^T of queries [64h, 64h+64) sits at columns 128 + 64h..
+            mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bq, mnmajor_step(kk)), kIdescKV,
                    (t > 0 || kk > 0));
-            if (more && kk < D / 16)
-              mma_ss(tDP, desc_add(dV, kmajor_step(kk, kBlk)), desc_add(bdo, kmajor_step(kk, kBlk)), kIdescSq, kk > 0);
-          }
         }
         tc_commit(&qdo_empty[st]);
-        if (more) tc_commit(dp_full);
+        if (more) issue_dp(t + 1);
       }
       if (ok) tc_commit(acc_done);
       tc_commit(drain);
@@ -362,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Np = nblk * kBlk;
     const float *lse2_h = p.lse2 + static_cast<size_t>(bh) * Np;
     const float *delta_h = p.delta + static_cast<size_t>(bh) * Np;
-    const uint32_t ds_tile = smem_addr(sDS);
     const bool key_ok = key < N;
     const int c0 = half * 64;  // first query column of this half
     bool ok = true;
@@ -423,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       warp_arrive(p_ready);
 
-      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 into the swizzled dS^T tile.
+      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 pairs over this half's own,
+      // already read, dP^T columns.
       ok = mbar_wait(dp_full, t & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -452,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
           dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
         }
-        store_row_sw128(ds_tile, r, c0 + ch * 32, dk);
+        tmem_st16(tDP + c0 + ch * 16, dk);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       warp_arrive(ds_ready);
     }
@@ -486,16 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DqLayout {
   static constexpr int kSlabs = D / 64;
-  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr int kKStages = 3, kVStages = 3;
   static constexpr uint32_t kTile = kBlk * D * 2;  // one [128][D] bf16 tile
-  // Q resident, K in a 3-stage ring, V in a 2-stage ring, one [128][128]
-  // bf16 dS tile.  dO lives in TMEM (the A operand of dP = dO V^T), which
-  // frees the shared memory for the third K stage.
+  // Q resident, K and V in 3-stage rings.  dO and dS live in TMEM (the A
+  // operands of dP = dO V^T and dQ = dS K), which frees the shared memory
+  // for the third stages.
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kTile;
   static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
-  static constexpr uint32_t kOffDS = kOffV + kVStages * kTile;
-  static constexpr uint32_t kOffBar = kOffDS + kBlk * kBlk * 2;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
   static constexpr int kNumBars = 24;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffMisc + 16;
@@ -503,13 +474,15 @@ struct DqLayout {
   static_assert(kSmemRequest <= 232448, "shared memory budget");
 };
 
-// TMEM columns: S [0,128) (lane = query row), dP [128,256), dQ [256,256+D),
-// dO [384, 384+D/2) as bf16 pairs.
-// MMA order per key block j:  S(j+1), [dQ(j) | dP(j+1)]
-// ([a | b]: the MMAs of two products with different accumulators issued
-// alternately) so the rows form P(j+1) while dQ(j) and dP(j+1) run and
-// dS(j+1) while S(j+2) runs.  K(j) is read by S(j) and, last, by dQ(j); the
-// third K stage lets K(j+2) load while dQ(j) still holds K(j).
+// TMEM columns: S [0,128) (lane = query row), dP [128,256) (dS of keys
+// [64h, 64h+64) as bf16 pairs over columns [128+64h, 128+64h+32), written by
+// the rows over dP they have already read), dQ [256,256+D), dO
+// [384, 384+D/2) as bf16 pairs.
+// MMA order per key block j:  S(j+1), dQ(j), dP(j+1)
+// so the rows form P(j+1) while dQ(j) and dP(j+1) run and dS(j+1) while
+// S(j+2) runs; dP(j+1) overwrites dS(j) after dQ(j) has read it (the tensor
+// core runs the products in order).  K(j) is read by S(j) and, last, by
+// dQ(j); the third K stage lets K(j+2) load while dQ(j) still holds K(j).
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -532,10 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *dp_full = s_full + 1;
   uint64_t *s_free = dp_full + 1;
   uint64_t *ds_ready = s_free + 1;
-  uint64_t *ds_free = ds_ready + 1;
-  uint64_t *dq_done = ds_free + 1;
+  uint64_t *dq_done = ds_ready + 1;
   uint64_t *drain = dq_done + 1;
-  static_assert(2 + 2 * SK + 2 * SV + 7 <= L::kNumBars, "barrier slots");
+  static_assert(2 + 2 * SK + 2 * SV + 6 <= L::kNumBars, "barrier slots");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
   const WaitCtl ctl{abort_flag, p.status};
@@ -572,7 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(s_free, kRowWarps);
     mbar_init(ds_ready, kRowWarps);
-    mbar_init(ds_free, 1);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -590,7 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sQ = smem + L::kOffQ;
   uint8_t *sK = smem + L::kOffK;
   uint8_t *sV = smem + L::kOffV;
-  uint8_t *sDS = smem + L::kOffDS;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers
@@ -636,12 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kBlk, kBlk, false, false);  // S, dP
       constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, false, true);      // dQ
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV), aDS = smem_addr(sDS);
+      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ, tDO = tmem + kColDO;
 
       // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
       // a compile-time step offset (all issue loops are unrolled).
-      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dDS = sdesc_sw128(aDS, 16, 1024);
+      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024);
       auto k_kmaj = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, 16, 1024); };
       auto k_mn = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, kBlk * 128, 1024); };
       auto v_kmaj = [&](int j) { return sdesc_sw128(aV + (j % SV) * L::kTile, 16, 1024); };
@@ -679,26 +649,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(j + 1);
         }
-        // dQ += dS K_j (dS K-major over keys; K_j MN-major over d) once dS(j)
-        // is in smem, interleaved with dP(j+1) (the rows have read dP(j))
+        // dQ += dS K_j (dS from TMEM over the dP columns; K_j MN-major over
+        // d) once the rows have written dS(j), then dP(j+1) over it
         if (!(ok = mbar_wait(ds_ready, j & 1, ctl, kSiteDsReady))) break;
         if (more && !(ok = mbar_wait(&v_full[(j + 1) % SV], ((j + 1) / SV) & 1, ctl, kSiteVFull))) break;
         tc_fence_after();
         {
-          const uint64_t bk = k_mn(j), bv = more ? v_kmaj(j + 1) : 0;
+          const uint64_t bk = k_mn(j);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk) {
-            mma_ss(tDQ, desc_add(dDS, kmajor_step(kk, kBlk)), desc_add(bk, mnmajor_step(kk)), kIdescQ,
+          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS of keys [64h, 64h+64) sits at columns 128 + 64h..
+            mma_ts(tDQ, tDP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bk, mnmajor_step(kk)), kIdescQ,
                    (j > 0 || kk > 0));
-            if (more && kk < D / 16) dp_step(bv, kk);
-          }
         }
+        tc_commit(&k_empty[j % SK]);
         if (more) {
+          const uint64_t bv = v_kmaj(j + 1);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
           tc_commit(dp_full);
           tc_commit(&v_empty[(j + 1) % SV]);
         }
-        tc_commit(ds_free);
-        tc_commit(&k_empty[j % SK]);
       }
       if (ok) tc_commit(dq_done);
       tc_commit(drain);
@@ -716,7 +686,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + qrow;
     const float lse2 = p.lse2[srow];  // +inf on padding rows: P = 0
     const float dlt = p.delta[srow];
-    const uint32_t ds_tile = smem_addr(sDS);
     const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
     const int c0 = half * 64;  // first key column of this half
     bool ok = true;
@@ -775,9 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // Phase 2: dS = P o (dP - D) -> bf16 into the swizzled [query][key] tile.
+      // Phase 2: dS = P o (dP - D) -> bf16 pairs over this half's own,
+      // already read, dP columns (dQ(j-1) has read dS(j-1) from there: it
+      // ran before dP(j)).
       ok = mbar_wait(dp_full, j & 1, ctl, kSiteSFull);
-      if (ok && j > 0) ok = mbar_wait(ds_free, (j - 1) & 1, ctl, kSiteDsReady);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -798,9 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 ds = fmul2(pf[ch * 16 + e / 2], g);
           dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
-        store_row_sw128(ds_tile, r, c0 + ch * 32, dsv);
+        tmem_st16(tDP + c0 + ch * 16, dsv);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       warp_arrive(ds_ready);
     }
