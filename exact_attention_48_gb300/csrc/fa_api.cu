@@ -170,6 +170,7 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     owned = true;
   }
   BwdParams p{};
+  p.q = static_cast<const __nv_bfloat16 *>(q);
   p.o = static_cast<const __nv_bfloat16 *>(o);
   p.dout = static_cast<const __nv_bfloat16 *>(dO);
   p.lse = lse;

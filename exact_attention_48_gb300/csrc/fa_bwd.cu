@@ -458,13 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DqLayout {
   static constexpr int kSlabs = D / 64;
-  static constexpr int kKStages = 3, kVStages = 3;
+  static constexpr int kKStages = 4, kVStages = 3;
   static constexpr uint32_t kTile = kBlk * D * 2;  // one [128][D] bf16 tile
-  // Q resident, K and V in 3-stage rings.  dO and dS live in TMEM (the A
-  // operands of dP = dO V^T and dQ = dS K), which frees the shared memory
-  // for the third stages.
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kTile;
+  // K in a 4-stage ring, V in a 3-stage ring.  Q, dO and dS live in TMEM
+  // (the A operands of S = Q K^T, dP = dO V^T and dQ = dS K), which leaves
+  // the shared memory to the rings.
+  static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
   static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
   static constexpr int kNumBars = 24;
@@ -477,7 +476,8 @@ struct DqLayout {
 // TMEM columns: S [0,128) (lane = query row), dP [128,256) (dS of keys
 // [64h, 64h+64) as bf16 pairs over columns [128+64h, 128+64h+32), written by
 // the rows over dP they have already read), dQ [256,256+D), dO
-// [384, 384+D/2) as bf16 pairs.
+// [384, 384+D/2) and Q [448, 448+D/2) as bf16 pairs (copied in once by the
+// rows).  Every product then reads only its B operand from shared memory.
 // MMA order per key block j:  S(j+1), dQ(j), dP(j+1)
 // so the rows form P(j+1) while dQ(j) and dP(j+1) run and dS(j+1) while
 // S(j+2) runs; dP(j+1) overwrites dS(j) after dQ(j) has read it (the tensor
@@ -490,13 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const BwdParams p) {
   using L = DqLayout<D>;
   constexpr int SK = L::kKStages, SV = L::kVStages;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDO = 384;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDO = 384, kColQ = 448;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-  uint64_t *q_full = bars;
-  uint64_t *do_ready = q_full + 1;    // dO written to TMEM by the rows
+  uint64_t *do_ready = bars;          // Q and dO written to TMEM by the rows
   uint64_t *k_full = do_ready + 1;    // [SK]
   uint64_t *k_empty = k_full + SK;    // [SK]
   uint64_t *v_full = k_empty + SK;    // [SV]
@@ -530,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv = CAUSAL ? (iblk + 1) : nblk;  // key blocks 0 .. n_kv-1
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     mbar_init(do_ready, kRowWarps);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
@@ -558,19 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t *sQ = smem + L::kOffQ;
   uint8_t *sK = smem + L::kOffK;
   uint8_t *sV = smem + L::kOffV;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
-      // Q once, then the K ring
-      tma_prefetch_desc(&tm_q);
+      // the K ring
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(q_full, L::kTile);
-#pragma unroll
-      for (int s = 0; s < L::kSlabs; ++s) tma_load_3d(sQ + s * kBlk * 128, &tm_q, q_full, s * 64, iblk * kBlk, bh);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % SK;
@@ -581,10 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, j * kBlk, bh);
         issued = j + 1;
       }
-      if (*abort_flag) {
-        mbar_drain(q_full, 0);
+      if (*abort_flag)
         for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
-      }
     } else if (lane == 1) {
       // the V ring
       tma_prefetch_desc(&tm_v);
@@ -606,22 +597,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kBlk, kBlk, false, false);  // S, dP
       constexpr uint32_t kIdescQ = idesc_bf16(kBlk, D, false, true);      // dQ
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ, tDO = tmem + kColDO;
+      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ, tDO = tmem + kColDO,
+                     tQ = tmem + kColQ;
 
       // Descriptors: fixed tiles once, ring tiles per stage; every MMA adds
       // a compile-time step offset (all issue loops are unrolled).
-      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024);
       auto k_kmaj = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, 16, 1024); };
       auto k_mn = [&](int j) { return sdesc_sw128(aK + (j % SK) * L::kTile, kBlk * 128, 1024); };
       auto v_kmaj = [&](int j) { return sdesc_sw128(aV + (j % SV) * L::kTile, 16, 1024); };
 
-      // S(j) = Q K_j^T (both K-major over d)
+      // S(j) = Q K_j^T (Q from TMEM, K_j K-major over d)
       auto issue_s = [&](int j) {
         const uint64_t bk = k_kmaj(j);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tS, desc_add(dQ, kmajor_step(kk, kBlk)), desc_add(bk, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
+          mma_ts(tS, tQ + kk * 8, desc_add(bk, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
         tc_commit(s_full);
       };
       // one K step of dP(j) = dO V_j^T (dO from TMEM, V_j K-major over d)
@@ -629,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts(tDP, tDO + kk * 8, desc_add(bv, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
       };
 
-      bool ok = mbar_wait(q_full, 0, ctl, kSiteQFull) && mbar_wait(&k_full[0], 0, ctl, kSiteKFull) &&
+      bool ok = mbar_wait(&k_full[0], 0, ctl, kSiteKFull) &&
                 mbar_wait(&v_full[0], 0, ctl, kSiteVFull) && mbar_wait(do_ready, 0, ctl, kSiteDoFull);
       if (ok) {
         tc_fence_after();
@@ -690,22 +681,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = half * 64;  // first key column of this half
     bool ok = true;
 
-    // dO row -> TMEM (bf16 pairs over D/2 columns): the A operand of dP.
+    // Q and dO rows -> TMEM (bf16 pairs over D/2 columns each): the A
+    // operands of S and dP.  The two halves share the 64-element pieces.
     {
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.dout + (static_cast<size_t>(bh) * N + qrow) * D);
+      const size_t roff = (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        if ((hh & 1) != half) continue;  // the two halves share the 64-element pieces
-        uint32_t v[32];
+      for (int m = 0; m < 2; ++m) {
+        const uint4 *src = reinterpret_cast<const uint4 *>((m ? p.dout : p.q) + roff);
+        const uint32_t col = m ? kColDO : kColQ;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = qrow < N ? src[hh * 8 + u] : make_uint4(0, 0, 0, 0);
-          v[4 * u] = x.x;
-          v[4 * u + 1] = x.y;
-          v[4 * u + 2] = x.z;
-          v[4 * u + 3] = x.w;
+        for (int hh = 0; hh < D / 64; ++hh) {
+          if (((hh + m) & 1) != half) continue;
+          uint32_t v[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = qrow < N ? src[hh * 8 + u] : make_uint4(0, 0, 0, 0);
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
+          }
+          tmem_st32(tmem + col + lane_base + hh * 32, v);
         }
-        tmem_st32(tmem + kColDO + lane_base + hh * 32, v);
       }
       tmem_st_wait();
       tc_fence_before();

@@ -40,6 +40,7 @@ struct FwdParams {
 };
 
 struct BwdParams {
+  const __nv_bfloat16 *q;     // [BH, N, d]
   const __nv_bfloat16 *o;     // [BH, N, d]
   const __nv_bfloat16 *dout;  // [BH, N, d]
   const float *lse;           // [BH, N]
