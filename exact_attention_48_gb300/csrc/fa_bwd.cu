@@ -120,7 +120,11 @@ struct BwdLayout {
   static constexpr uint32_t kOffRes1 = kOffRes0 + kTile;
   static constexpr uint32_t kOffRing0 = kOffRes1 + kTile;             // kStages tiles
   static constexpr uint32_t kOffRing1 = kOffRing0 + kStages * kTile;  // kStages tiles
-  static constexpr uint32_t kOffBar = kOffRing1 + kStages * kTile;
+  // per ring stage, the query block's row statistics: lse*log2(e) [128]
+  // then D [128] (fp32), loaded with Q and dO
+  static constexpr uint32_t kStatBytes = 2 * kBlk * 4;
+  static constexpr uint32_t kOffStats = kOffRing1 + kStages * kTile;
+  static constexpr uint32_t kOffBar = kOffStats + kStages * kStatBytes;
   static constexpr int kNumBars = 16;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffMisc + 16;
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sV = smem + L::kOffRes1;
   uint8_t *sQ = smem + L::kOffRing0;
   uint8_t *sDO = smem + L::kOffRing1;
+  uint8_t *sStats = smem + L::kOffStats;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -232,13 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < n_q; ++t) {
         const int st = t % S;
         if (!mbar_wait(&qdo_empty[st], ((t / S) & 1) ^ 1, ctl, kSiteDoEmpty)) break;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile);
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kStatBytes);
         const int i = i0 + t;
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s) {
           tma_load_3d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, i * kBlk, bh);
           tma_load_3d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, i * kBlk, bh);
         }
+        const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + static_cast<size_t>(i) * kBlk;
+        bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
+        bulk_load(sStats + st * L::kStatBytes + kBlk * 4, p.delta + srow, kBlk * 4, &qdo_full[st]);
         issued = t + 1;
       }
       if (*abort_flag) {
@@ -331,26 +339,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
-    const int Np = nblk * kBlk;
-    const float *lse2_h = p.lse2 + static_cast<size_t>(bh) * Np;
-    const float *delta_h = p.delta + static_cast<size_t>(bh) * Np;
     const bool key_ok = key < N;
     const int c0 = half * 64;  // first query column of this half
     bool ok = true;
-    if (half == 0 && wq == 0 && lane < 8) prefetch_l1((lane < 4 ? lse2_h : delta_h) + i0 * kBlk + (lane & 3) * 32);
 
     for (int t = 0; t < n_q; ++t) {
       const int i = i0 + t;
-      // per-query statistics of this block (same for every thread: L1 broadcasts)
-      const float4 *lse4 = reinterpret_cast<const float4 *>(lse2_h + i * kBlk + c0);
-      const float4 *del4 = reinterpret_cast<const float4 *>(delta_h + i * kBlk + c0);
+      // per-query statistics of this block, in shared memory with Q and dO
+      // (same address in every thread: broadcast reads)
+      const float *stats = reinterpret_cast<const float *>(sStats + (t % S) * L::kStatBytes);
+      const float4 *lse4 = reinterpret_cast<const float4 *>(stats + c0);
+      const float4 *del4 = reinterpret_cast<const float4 *>(stats + kBlk + c0);
       const bool diag = CAUSAL && (i == jblk);
-      // the next block's statistics into L1 now (8 lines of 128 bytes)
-      if (t + 1 < n_q && half == 0 && wq == 0 && lane < 8)
-        prefetch_l1((lane < 4 ? lse2_h : delta_h) + (i + 1) * kBlk + (lane & 3) * 32);
 
       // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + 32).
-      ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull);
+      // (The stage's copies are complete once S^T(t) is; the rows wait on
+      // them too so that the statistics' copy is visible to their loads.
+      // The stage cannot be refilled before ds_ready(t).)
+      ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull) &&
+           mbar_wait(&qdo_full[t % S], (t / S) & 1, ctl, kSiteDoFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int qh = ch * 32 + e;  // query column within the half
-          const float4 l4 = __ldg(lse4 + qh / 4);
+          const float4 l4 = lse4[qh / 4];
           const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), make_float2(c, c),
                                    make_float2(-l4.x, -l4.y));
           const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int qh = ch * 32 + e;
-          const float4 d4 = __ldg(del4 + qh / 4);
+          const float4 d4 = del4[qh / 4];
           const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
                                    make_float2(-d4.x, -d4.y));
           const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
