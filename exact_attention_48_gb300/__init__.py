@@ -7,9 +7,11 @@ CPU fallback.
 from .binding import (  # noqa: F401
     FaError,
     fa_bwd,
+    fa_bwd_strided,
     fa_bwd_workspace_bytes,
     fa_device_status,
     fa_fwd,
+    fa_fwd_strided,
     library,
     status_string,
 )

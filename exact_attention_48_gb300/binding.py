@@ -63,6 +63,12 @@ def library(path: str | None = None):
             lib.fa_debug_last_wait_site.restype = i
             lib.fa_debug_time_next_bwd.argtypes = [vp, vp, vp]
             lib.fa_debug_time_next_bwd.restype = i
+            p64 = ctypes.POINTER(ctypes.c_int64)
+            lib.fa_fwd_strided.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, i, i, i, i, i, f, vp]
+            lib.fa_fwd_strided.restype = i
+            lib.fa_bwd_strided.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, p64, vp, p64,
+                                           vp, p64, i, i, i, i, i, f, vp, sz, vp]
+            lib.fa_bwd_strided.restype = i
             lib.fa_status_string.argtypes = [i]
             lib.fa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -88,6 +94,81 @@ def _check_qkv(name, t, shape=None):
         raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_view(name, t, shape=None):
+    """A [B, H, N, d] bf16 CUDA view with contiguous d (any other strides)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 4 or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be a [B, H, N, d] view with contiguous d")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _strides(t):
+    return (ctypes.c_int64 * 3)(*t.stride()[:3])
+
+
+def fa_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+    """fa_fwd on [B, H, N, d] views of any layout whose d is contiguous
+    (e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor, or the q, k, v
+    slices of a packed projection).  ``o`` defaults to a contiguous tensor."""
+    _check_view("q", q)
+    B, H, N, d = q.shape
+    _check_view("k", k, q.shape)
+    _check_view("v", v, q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty(q.shape, device=q.device, dtype=q.dtype)
+    else:
+        _check_view("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    rc = library().fa_fwd_strided(q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v),
+                                  o.data_ptr(), _strides(o), lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                                  float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_strided")
+    return o, lse
+
+
+def fa_bwd_strided(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+                   dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """fa_bwd on [B, H, N, d] views of any layout whose d is contiguous;
+    dq, dk, dv default to contiguous tensors."""
+    _check_view("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_view(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    new = lambda: torch.empty(q.shape, device=q.device, dtype=q.dtype)  # noqa: E731
+    dq = new() if dq is None else dq
+    dk = new() if dk is None else dk
+    dv = new() if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_view(name, t, q.shape)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = library().fa_bwd_strided(q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v),
+                                  o.data_ptr(), _strides(o), dout.data_ptr(), _strides(dout), lse.data_ptr(),
+                                  dq.data_ptr(), _strides(dq), dk.data_ptr(), _strides(dk), dv.data_ptr(),
+                                  _strides(dv), B, H, N, d, int(bool(causal)), float(scale), ws_ptr, ws_bytes,
+                                  _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_strided")
+    return dq, dk, dv
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):

@@ -33,19 +33,113 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [BH, N, d] bf16 viewed as 3-D (d, N, BH); one box is 64 columns (128
-// bytes, the swizzle span) x 128 rows of one head.  Rows past N read as 0.
-bool encode_bhnd(CUtensorMap *map, const void *base, int BH, int N, int d) {
+// A [B, H, N, d] bf16 tensor with element strides s (d contiguous) viewed
+// as 4-D (d, N, H, B); one box is 64 columns (128 bytes, the swizzle span) x
+// 128 rows of one head.  Rows past N read as 0.
+bool encode_map(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * 2, static_cast<cuuint64_t>(s.h) * 2,
+                           static_cast<cuuint64_t>(s.b) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+Strides contiguous(int H, int N, int d) {
+  return Strides{static_cast<long long>(H) * N * d, static_cast<long long>(N) * d, d};
+}
+
+// A caller's strides made usable: the stride of an extent-1 dimension is
+// never used, so it is replaced by a harmless valid value; then every
+// stride must be positive and a multiple of 8 elements (16 bytes: TMA and
+// the 16-byte row accesses).  False if the layout is not supported.
+bool normalise(const int64_t *in, int B, int H, int N, int d, Strides *out) {
+  if (!in) return false;
+  Strides s{in[0], in[1], in[2]};
+  if (N == 1) s.n = d;  // d is 64 or 128: a multiple of 8
+  if (H == 1) s.h = s.n * N;
+  if (B == 1) s.b = s.h * H;
+  const long long lim = 1LL << 40;  // TMA strides are below 2^40 bytes
+  for (long long v : {s.b, s.h, s.n})
+    if (v <= 0 || (v & 7) || v >= lim / 2) return false;
+  *out = s;
+  return true;
+}
+
+// Address span [lo, hi) of the elements of a strided tensor.
+void span(const void *base, int B, int H, int N, int d, const Strides &s, uintptr_t *lo, uintptr_t *hi) {
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(base);
+  const long long last = (B - 1) * s.b + (H - 1) * s.h + (N - 1) * s.n + d;
+  *lo = b0;
+  *hi = b0 + static_cast<uintptr_t>(last) * 2;
+}
+
+// No two elements of the tensor share an address (each stride covers the
+// extent of the smaller ones): required of the outputs.
+bool injective(int B, int H, int N, int d, const Strides &s) {
+  struct Dim { long long stride, extent; } dims[3] = {{s.b, B}, {s.h, H}, {s.n, N}};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (dims[j].stride < dims[i].stride) {
+        Dim t = dims[i];
+        dims[i] = dims[j];
+        dims[j] = t;
+      }
+  long long covered = d;  // the contiguous d elements
+  for (const Dim &x : dims) {
+    if (x.extent == 1) continue;
+    if (x.stride < covered) return false;
+    covered = x.stride * x.extent;
+  }
+  return true;
+}
+
+bool spans_overlap(uintptr_t alo, uintptr_t ahi, uintptr_t blo, uintptr_t bhi) { return alo < bhi && blo < ahi; }
+
+// Two tensors with the same strides s, whose layout is injective (each
+// stride at least the extent of the smaller ones), and bases `delta`
+// elements apart share an element iff delta = sum_k a_k s_k + c with
+// |a_k| < extent_k and |c| < d.  With nested strides only the two integer
+// quotients next to delta / s_k can work at each level, so this small
+// search is exact.  (It lets the slices of one packed buffer, such as the
+// q, k, v gradients of a [B, N, 3, H, d] projection, be outputs together.)
+bool lattice_hit(long long rem, const long long (*dims)[2], int k, int d) {
+  if (k == 3) return rem > -d && rem < d;
+  const long long st = dims[k][0], ext = dims[k][1];
+  const long long q = rem / st;
+  for (long long a = q - 1; a <= q + 1; ++a)
+    if (a > -ext && a < ext && lattice_hit(rem - a * st, dims, k + 1, d)) return true;
+  return false;
+}
+
+// Whether two tensors of [B, H, N, d] may share an element.  Exact when
+// both have the same injective strides; otherwise whether their address
+// spans overlap.
+bool may_overlap(const void *a, const Strides &sa, const void *b, const Strides &sb, int B, int H, int N, int d) {
+  uintptr_t alo, ahi, blo, bhi;
+  span(a, B, H, N, d, sa, &alo, &ahi);
+  span(b, B, H, N, d, sb, &blo, &bhi);
+  if (!spans_overlap(alo, ahi, blo, bhi)) return false;
+  const bool same = sa.b == sb.b && sa.h == sb.h && sa.n == sb.n;
+  if (!same || !injective(B, H, N, d, sa)) return true;
+  long long dims[3][2] = {{sa.b, B}, {sa.h, H}, {sa.n, N}};
+  for (int i = 0; i < 3; ++i)  // descending strides
+    for (int j = i + 1; j < 3; ++j)
+      if (dims[j][0] > dims[i][0])
+        for (int c = 0; c < 2; ++c) {
+          const long long t = dims[i][c];
+          dims[i][c] = dims[j][c];
+          dims[j][c] = t;
+        }
+  const long long delta_bytes = static_cast<long long>(reinterpret_cast<uintptr_t>(b) - reinterpret_cast<uintptr_t>(a));
+  if (delta_bytes % 2) return true;
+  return lattice_hit(delta_bytes / 2, dims, 0, d);
 }
 
 int *status_ptr() {
@@ -72,10 +166,6 @@ thread_local cudaEvent_t t_bwd_ev[3] = {nullptr, nullptr, nullptr};
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + nb && y < x + na;
-}
 
 }  // namespace
 }  // namespace fa
@@ -96,71 +186,96 @@ const char *fa_status_string(fa_status_t s) {
   return "unknown status";
 }
 
-fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
-                   int causal, float scale, cudaStream_t stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+fa_status_t fwd_impl(const void *q, const Strides &sq, const void *k, const Strides &sk, const void *v,
+                     const Strides &sv, void *o, const Strides &so, float *lse, int B, int H, int N, int d,
+                     int causal, float scale, cudaStream_t stream) {
   fa_status_t st = check_common(B, H, N, d, causal, scale);
   if (st != FA_OK) return st;
   const void *ptrs[5] = {q, k, v, o, lse};
   for (const void *x : ptrs)
     if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
-  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
-  for (const void *in : {q, k, v})
-    if (overlaps(in, tb, o, tb) || overlaps(in, tb, lse, lb)) return FA_ERR_INVALID_ARGUMENT;
-  if (overlaps(o, tb, lse, lb)) return FA_ERR_INVALID_ARGUMENT;
+  if (!injective(B, H, N, d, so)) return FA_ERR_INVALID_ARGUMENT;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  uintptr_t olo, ohi, llo = reinterpret_cast<uintptr_t>(lse), lhi = llo + lb;
+  span(o, B, H, N, d, so, &olo, &ohi);
+  const void *ins[3] = {q, k, v};
+  const Strides *ins_s[3] = {&sq, &sk, &sv};
+  for (int i = 0; i < 3; ++i) {
+    uintptr_t lo, hi;
+    span(ins[i], B, H, N, d, *ins_s[i], &lo, &hi);
+    if (may_overlap(ins[i], *ins_s[i], o, so, B, H, N, d) || spans_overlap(lo, hi, llo, lhi))
+      return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (spans_overlap(olo, ohi, llo, lhi)) return FA_ERR_INVALID_ARGUMENT;
 
-  const int BH = B * H;
   CUtensorMap tq, tk, tv;
-  if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, N, d) || !encode_bhnd(&tv, v, BH, N, d))
+  if (!encode_map(&tq, q, B, H, N, d, sq) || !encode_map(&tk, k, B, H, N, d, sk) ||
+      !encode_map(&tv, v, B, H, N, d, sv))
     return FA_ERR_CUDA;
   FwdParams p{};
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
+  p.so = so;
+  p.H = H;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
-  p.BH = BH;
+  p.BH = B * H;
   p.num_qblk = (N + 255) / 256;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.neg = scale < 0.0f ? 1 : 0;
   return launch_fwd(d, causal != 0, tq, tk, tv, p, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (check_common(B, H, N, d, 0, 1.0f) != FA_OK) return 0;
-  const size_t padded_rows = static_cast<size_t>(B) * H * ((N + 127) / 128) * 128;
-  return 2 * round256(padded_rows * 4);
-}
-
-fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dO, const float *lse,
-                   void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal, float scale, void *workspace,
-                   size_t workspace_bytes, cudaStream_t stream) {
+fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Strides &sk, const void *v,
+                     const Strides &sv, const void *o, const Strides &so, const void *dO, const Strides &sdo,
+                     const float *lse, void *dq, const Strides &sdq, void *dk, const Strides &sdk, void *dv,
+                     const Strides &sdv, int B, int H, int N, int d, int causal, float scale, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
   fa_status_t st = check_common(B, H, N, d, causal, scale);
   if (st != FA_OK) return st;
   const void *ptrs[9] = {q, k, v, o, dO, lse, dq, dk, dv};
   for (const void *x : ptrs)
     if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
-  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
-  const void *ins[6] = {q, k, v, o, dO, lse};
-  const size_t in_sz[6] = {tb, tb, tb, tb, tb, lb};
   void *outs[3] = {dq, dk, dv};
-  for (int i = 0; i < 6; ++i)
-    for (void *out : outs)
-      if (overlaps(ins[i], in_sz[i], out, tb)) return FA_ERR_INVALID_ARGUMENT;
-  if (overlaps(dq, tb, dk, tb) || overlaps(dq, tb, dv, tb) || overlaps(dk, tb, dv, tb)) return FA_ERR_INVALID_ARGUMENT;
+  const Strides *outs_s[3] = {&sdq, &sdk, &sdv};
+  for (int i = 0; i < 3; ++i)
+    if (!injective(B, H, N, d, *outs_s[i])) return FA_ERR_INVALID_ARGUMENT;
+  uintptr_t in_lo[6], in_hi[6], out_lo[3], out_hi[3];
+  const void *ins[5] = {q, k, v, o, dO};
+  const Strides *ins_s[5] = {&sq, &sk, &sv, &so, &sdo};
+  for (int i = 0; i < 5; ++i) span(ins[i], B, H, N, d, *ins_s[i], &in_lo[i], &in_hi[i]);
+  in_lo[5] = reinterpret_cast<uintptr_t>(lse);
+  in_hi[5] = in_lo[5] + static_cast<size_t>(B) * H * N * 4;
+  for (int i = 0; i < 3; ++i) span(outs[i], B, H, N, d, *outs_s[i], &out_lo[i], &out_hi[i]);
+  for (int j = 0; j < 3; ++j) {
+    for (int i = 0; i < 5; ++i)
+      if (may_overlap(ins[i], *ins_s[i], outs[j], *outs_s[j], B, H, N, d)) return FA_ERR_INVALID_ARGUMENT;
+    if (spans_overlap(in_lo[5], in_hi[5], out_lo[j], out_hi[j])) return FA_ERR_INVALID_ARGUMENT;  // lse
+  }
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (may_overlap(outs[i], *outs_s[i], outs[j], *outs_s[j], B, H, N, d)) return FA_ERR_INVALID_ARGUMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (workspace) {
     if (workspace_bytes < need) return FA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID_ARGUMENT;
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
     for (int i = 0; i < 6; ++i)
-      if (overlaps(ins[i], in_sz[i], workspace, need)) return FA_ERR_INVALID_ARGUMENT;
-    for (void *out : outs)
-      if (overlaps(out, tb, workspace, need)) return FA_ERR_INVALID_ARGUMENT;
+      if (spans_overlap(in_lo[i], in_hi[i], wlo, whi)) return FA_ERR_INVALID_ARGUMENT;
+    for (int j = 0; j < 3; ++j)
+      if (spans_overlap(out_lo[j], out_hi[j], wlo, whi)) return FA_ERR_INVALID_ARGUMENT;
   }
 
   const int BH = B * H;
   CUtensorMap tq, tk, tv, tdo;
-  if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, N, d) || !encode_bhnd(&tv, v, BH, N, d) ||
-      !encode_bhnd(&tdo, dO, BH, N, d))
+  if (!encode_map(&tq, q, B, H, N, d, sq) || !encode_map(&tk, k, B, H, N, d, sk) ||
+      !encode_map(&tv, v, B, H, N, d, sv) || !encode_map(&tdo, dO, B, H, N, d, sdo))
     return FA_ERR_CUDA;
 
   void *ws = workspace;
@@ -180,6 +295,13 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
   p.dq = static_cast<__nv_bfloat16 *>(dq);
   p.dk = static_cast<__nv_bfloat16 *>(dk);
   p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.sq = sq;
+  p.so = so;
+  p.sdo = sdo;
+  p.sdq = sdq;
+  p.sdk = sdk;
+  p.sdv = sdv;
+  p.H = H;
   p.status = status_ptr();
   p.N = N;
   p.BH = BH;
@@ -193,6 +315,59 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     rc = FA_ERR_CUDA;
   if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   return rc;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+                   int causal, float scale, cudaStream_t stream) {
+  const Strides s = contiguous(H, N, d);
+  return fwd_impl(q, s, k, s, v, s, o, s, lse, B, H, N, d, causal, scale, stream);
+}
+
+fa_status_t fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                           const void *v, const int64_t *v_strides, void *o, const int64_t *o_strides, float *lse,
+                           int B, int H, int N, int d, int causal, float scale, cudaStream_t stream) {
+  fa_status_t st = check_common(B, H, N, d, causal, scale);
+  if (st != FA_OK) return st;
+  Strides sq, sk, sv, so;
+  if (!normalise(q_strides, B, H, N, d, &sq) || !normalise(k_strides, B, H, N, d, &sk) ||
+      !normalise(v_strides, B, H, N, d, &sv) || !normalise(o_strides, B, H, N, d, &so))
+    return FA_ERR_INVALID_ARGUMENT;
+  return fwd_impl(q, sq, k, sk, v, sv, o, so, lse, B, H, N, d, causal, scale, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_common(B, H, N, d, 0, 1.0f) != FA_OK) return 0;
+  const size_t padded_rows = static_cast<size_t>(B) * H * ((N + 127) / 128) * 128;
+  return 2 * round256(padded_rows * 4);
+}
+
+fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dO, const float *lse,
+                   void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal, float scale, void *workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  const Strides s = contiguous(H, N, d);
+  return bwd_impl(q, s, k, s, v, s, o, s, dO, s, lse, dq, s, dk, s, dv, s, B, H, N, d, causal, scale, workspace,
+                  workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                           const void *v, const int64_t *v_strides, const void *o, const int64_t *o_strides,
+                           const void *dO, const int64_t *dO_strides, const float *lse, void *dq,
+                           const int64_t *dq_strides, void *dk, const int64_t *dk_strides, void *dv,
+                           const int64_t *dv_strides, int B, int H, int N, int d, int causal, float scale,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  fa_status_t st = check_common(B, H, N, d, causal, scale);
+  if (st != FA_OK) return st;
+  Strides s[8];
+  const int64_t *in[8] = {q_strides, k_strides, v_strides, o_strides, dO_strides, dq_strides, dk_strides, dv_strides};
+  for (int i = 0; i < 8; ++i)
+    if (!normalise(in[i], B, H, N, d, &s[i])) return FA_ERR_INVALID_ARGUMENT;
+  return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7], B, H, N, d,
+                  causal, scale, workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_device_status(cudaStream_t stream) {

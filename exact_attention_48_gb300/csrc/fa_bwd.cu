@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   const int part = threadIdx.x % kTpr;
   float acc = 0.0f;
   if (real) {
-    const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row * D)[part];
-    const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row * D)[part];
+    const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row_offset(p.so, bh, p.H, q))[part];
+    const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row_offset(p.sdo, bh, p.H, q))[part];
     const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
     const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
 #pragma unroll
@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
 #pragma unroll
       for (int s = 0; s < L::kSlabs; ++s) {
-        tma_load_3d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, jblk * kBlk, bh);
-        tma_load_3d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, jblk * kBlk, bh);
+        tma_load_4d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, jblk * kBlk, bh % p.H, bh / p.H);
+        tma_load_4d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, jblk * kBlk, bh % p.H, bh / p.H);
       }
       int issued = 0;
       for (int t = 0; t < n_q; ++t) {
@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + t;
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s) {
-          tma_load_3d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, i * kBlk, bh);
-          tma_load_3d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, i * kBlk, bh);
+          tma_load_4d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, i * kBlk, bh % p.H,
+                      bh / p.H);
+          tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, i * kBlk, bh % p.H,
+                      bh / p.H);
         }
         const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + static_cast<size_t>(i) * kBlk;
         bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
@@ -444,11 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      const size_t row = static_cast<size_t>(bh) * N + key;
       if (half == 0)
-        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row * D, key_ok, 1.0f);
+        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row_offset(p.sdv, bh, p.H, key), key_ok, 1.0f);
       else
-        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row * D, key_ok, p.scale);
+        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row_offset(p.sdk, bh, p.H, key), key_ok, p.scale);
     }
   }
 
@@ -578,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], L::kTile);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, j * kBlk, bh);
+          tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, j * kBlk, bh % p.H, bh / p.H);
         issued = j + 1;
       }
       if (*abort_flag)
@@ -593,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&v_full[st], L::kTile);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, j * kBlk, bh);
+          tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, j * kBlk, bh % p.H, bh / p.H);
         issued = j + 1;
       }
       if (*abort_flag)
@@ -691,10 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q and dO rows -> TMEM (bf16 pairs over D/2 columns each): the A
     // operands of S and dP.  The two halves share the 64-element pieces.
     {
-      const size_t roff = (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const uint4 *src = reinterpret_cast<const uint4 *>((m ? p.dout : p.q) + roff);
+        const uint4 *src = reinterpret_cast<const uint4 *>(m ? p.dout + row_offset(p.sdo, bh, p.H, qrow)
+                                                             : p.q + row_offset(p.sq, bh, p.H, qrow));
         const uint32_t col = m ? kColDO : kColQ;
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh) {
@@ -786,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       store_acc_row<D / 2>(tmem + kColDQ + lane_base + half * (D / 2),
-                           p.dq + (static_cast<size_t>(bh) * N + qrow) * D + half * (D / 2), qrow < N, p.scale);
+                           p.dq + row_offset(p.sdq, bh, p.H, qrow) + half * (D / 2), qrow < N, p.scale);
     }
   }
 

@@ -232,7 +232,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     const float inv_l = 1.0f / lb_run;
     const int grow_row = a.grow0 + row;
     const bool store = grow_row < N;
-    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + grow_row) * D;
+    __nv_bfloat16 *orow = p.o + row_offset(p.so, bh, p.H, grow_row);
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t o[32];
@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = static_cast<int>(blockIdx.x) / p.num_qblk;
     qb = static_cast<int>(blockIdx.x) % p.num_qblk;
   }
+  const int bh_b = bh / p.H, bh_h = bh % p.H;  // batch and head of the tile (TMA coordinates)
   const int N = p.N;
   const int nkv_all = (N + kBN - 1) / kBN;
   const int n0 = CAUSAL ? min(2 * qb + 1, nkv_all) : nkv_all;  // key blocks of tile 0
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, qb * 2 * kBM + t * kBM, bh);
+          tma_load_4d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, qb * 2 * kBM + t * kBM, bh_h, bh_b);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
@@ -346,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, j * kBN, bh);
+          tma_load_4d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, j * kBN, bh_h, bh_b);
         k_issued = j + 1;
         if (!mbar_wait(&v_empty[st], ph ^ 1, ctl, kSiteVEmpty)) break;
         mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, j * kBN, bh);
+          tma_load_4d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, j * kBN, bh_h, bh_b);
         v_issued = j + 1;
       }
       if (*abort_flag) {

@@ -28,9 +28,22 @@ enum WaitSite : int {
   kSiteMmaDone,
 };
 
+// Element strides of a [B, H, N, d] bf16 tensor whose d elements are
+// contiguous: element (b, h, n, c) is at base + b*b + h*h + n*n + c.
+struct Strides {
+  long long b, h, n;
+};
+
+// Offset of row n of head bh (= b*H + h) of a strided tensor.
+__host__ __device__ inline long long row_offset(const Strides &s, int bh, int H, int n) {
+  return static_cast<long long>(bh / H) * s.b + static_cast<long long>(bh % H) * s.h + static_cast<long long>(n) * s.n;
+}
+
 struct FwdParams {
-  __nv_bfloat16 *o;   // [BH, N, d]
-  float *lse;         // [BH, N]
+  __nv_bfloat16 *o;   // [B, H, N, d] with strides so
+  float *lse;         // [BH, N] contiguous
+  Strides so;
+  int H;
   int *status;        // device status block (2 ints)
   int N;
   int BH;
@@ -40,15 +53,17 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  const __nv_bfloat16 *q;     // [BH, N, d]
-  const __nv_bfloat16 *o;     // [BH, N, d]
-  const __nv_bfloat16 *dout;  // [BH, N, d]
+  const __nv_bfloat16 *q;     // [B, H, N, d] with strides sq (likewise every bf16 tensor below)
+  const __nv_bfloat16 *o;
+  const __nv_bfloat16 *dout;
   const float *lse;           // [BH, N]
   float *delta;               // [BH, Np]  D = rowsum(dO * O), Np = 128 * num_blk, 0 past N
   float *lse2;                // [BH, Np]  lse * log2(e), +inf past N
-  __nv_bfloat16 *dq;          // [BH, N, d]
-  __nv_bfloat16 *dk;          // [BH, N, d]
-  __nv_bfloat16 *dv;          // [BH, N, d]
+  __nv_bfloat16 *dq;
+  __nv_bfloat16 *dk;
+  __nv_bfloat16 *dv;
+  Strides sq, so, sdo, sdq, sdk, sdv;
+  int H;
   int *status;
   int N;
   int BH;
@@ -57,8 +72,8 @@ struct BwdParams {
   float scale_log2;
 };
 
-// Three tensor maps over a [BH, N, d] bf16 tensor viewed as 3-D (d, N, BH),
-// box (64, 128, 1), 128-byte swizzle.
+// Tensor maps over [B, H, N, d] bf16 tensors viewed as 4-D (d, N, H, B)
+// with the tensors' strides, box (64, 128, 1, 1), 128-byte swizzle.
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 

@@ -16,7 +16,9 @@
  *
  * Conventions shared by every call below.
  *  - Tensors q, k, v, o, dO, dq, dk, dv are bf16, contiguous [B, H, N, d]
- *    (d fastest).  lse is fp32, contiguous [B, H, N].  All pointers are
+ *    (d fastest), except in the *_strided calls, which take any layout
+ *    whose d elements are contiguous.  lse is fp32, contiguous [B, H, N].
+ *    All pointers are
  *    device pointers owned by the caller, 16-byte aligned, non-null, and
  *    the library keeps none of them after the call returns.
  *  - B, H, N >= 1; d is 64 or 128 (FA_ERR_UNSUPPORTED otherwise);
@@ -39,6 +41,7 @@
 #define FA_H_
 
 #include <stddef.h>
+#include <stdint.h>
 #include <cuda_runtime_api.h>
 
 #if defined(__GNUC__)
@@ -101,6 +104,38 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
                    const void *dO, const float *lse, void *dq, void *dk, void *dv,
                    int B, int H, int N, int d, int causal, float scale,
                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Strided layouts.  The same two passes on tensors in any layout whose d
+ * elements are contiguous: element (b, h, n, c) of a tensor lies at
+ *     base + b * strides[0] + h * strides[1] + n * strides[2] + c
+ * (strides in elements, int64, one array of three per tensor).  This covers
+ * [B, N, H, d] ("BNHD", the layout of many frameworks' projections), the
+ * q, k, v slices of one packed [B, N, 3, H, d] projection, and any padded
+ * row pitch; the page "FlashAttention-2 (DE)" (systems-analysis.info),
+ * section "Anwendung und Integration in das Oekosystem", names the
+ * frameworks this is for.  Rules: every stride of a dimension of extent > 1
+ * is a positive multiple of 8 elements (16 bytes) below 2^39 (the stride of
+ * an extent-1 dimension is ignored); inputs may share memory with each
+ * other (a packed projection); each output's elements are all distinct and
+ * no output overlaps an input, another output or the workspace (checked on
+ * the address ranges spanned).  lse stays contiguous [B, H, N].  Everything
+ * else is as in fa_fwd / fa_bwd; with contiguous strides the results are
+ * bitwise those of fa_fwd / fa_bwd.
+ */
+FA_API fa_status_t fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k,
+                                  const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                                  void *o, const int64_t *o_strides, float *lse, int B, int H, int N,
+                                  int d, int causal, float scale, cudaStream_t stream);
+
+FA_API fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const void *k,
+                                  const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                                  const void *o, const int64_t *o_strides, const void *dO,
+                                  const int64_t *dO_strides, const float *lse, void *dq,
+                                  const int64_t *dq_strides, void *dk, const int64_t *dk_strides,
+                                  void *dv, const int64_t *dv_strides, int B, int H, int N, int d,
+                                  int causal, float scale, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
 
 /*
  * Size in bytes of the fixed device array that fa_bwd_noalloc uses as its

@@ -112,3 +112,43 @@ def test_workspace_bytes(lib):
     assert b == 2 * a
     assert lib.fa_bwd_workspace_bytes(1, 1, 128, 96) == 0
     assert lib.fa_bwd_workspace_bytes(0, 1, 128, 64) == 0
+
+
+def _s(*v):
+    return (ctypes.c_int64 * 3)(*v)
+
+
+def _fwd_strided(lib, *, qs=None, os_=None, o=FAKE + (3 << 30), B=1, H=2, N=128, d=64):
+    c = _s(H * N * d, N * d, d)
+    return lib.fa_fwd_strided(FAKE, qs or c, FAKE + (1 << 30), c, FAKE + (2 << 30), c, o, os_ or c,
+                              FAKE + (4 << 30), B, H, N, d, 0, 0.125, None)
+
+
+def test_fwd_strided_rejects(lib):
+    H, N, d = 2, 128, 64
+    assert _fwd_strided(lib, qs=_s(H * N * d, N * d, d + 4)) == FA_ERR_INVALID_ARGUMENT   # not a multiple of 8
+    assert _fwd_strided(lib, qs=_s(H * N * d, 0, d)) == FA_ERR_INVALID_ARGUMENT           # zero stride, extent 2
+    assert _fwd_strided(lib, os_=_s(H * N * d, N * d, 8)) == FA_ERR_INVALID_ARGUMENT      # rows of o overlap
+    assert _fwd_strided(lib, os_=_s(H * N * d, N * d // 2, d)) == FA_ERR_INVALID_ARGUMENT  # heads of o overlap
+    assert _fwd_strided(lib, o=FAKE + (1 << 30) + 256) == FA_ERR_INVALID_ARGUMENT        # o inside k
+    assert lib.fa_fwd_strided(FAKE, None, FAKE, None, FAKE, None, FAKE, None, FAKE, 1, 2, 128, 64, 0, 0.125,
+                              None) == FA_ERR_INVALID_ARGUMENT                             # no strides
+    assert _fwd_strided(lib, d=96) == FA_ERR_UNSUPPORTED
+
+
+def test_bwd_strided_rejects(lib):
+    H, N, d = 2, 128, 64
+    c = _s(H * N * d, N * d, d)
+
+    def call(dq=FAKE + (10 << 30), dqs=c, dk=FAKE + (11 << 30), dks=c):
+        return lib.fa_bwd_strided(FAKE, c, FAKE + (1 << 30), c, FAKE + (2 << 30), c, FAKE + (3 << 30), c,
+                                  FAKE + (4 << 30), c, FAKE + (5 << 30), dq, dqs, dk, dks, FAKE + (12 << 30), c,
+                                  1, H, N, d, 0, 0.125, None, 0, None)
+    assert call(dk=FAKE + (10 << 30) + 4096) == FA_ERR_INVALID_ARGUMENT                  # dk overlaps dq
+    assert call(dks=_s(H * N * d, d, d)) == FA_ERR_INVALID_ARGUMENT                      # dk rows collide
+    assert call(dq=FAKE + (2 << 30)) == FA_ERR_INVALID_ARGUMENT                          # dq is v
+    assert call(dqs=_s(H * N * d, N * d, 12)) == FA_ERR_INVALID_ARGUMENT                 # not a multiple of 8
+    # slices of one packed [B, N, 3, H, d] buffer: dk one head (d elements)
+    # after dq collides with dq's second head (a gap of H*d would not)
+    packed = _s(N * 3 * H * d, d, 3 * H * d)
+    assert call(dqs=packed, dk=FAKE + (10 << 30) + 2 * d, dks=packed) == FA_ERR_INVALID_ARGUMENT
