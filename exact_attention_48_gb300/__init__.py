@@ -8,10 +8,12 @@ from .binding import (  # noqa: F401
     FaError,
     fa_bwd,
     fa_bwd_strided,
+    fa_bwd_varlen,
     fa_bwd_workspace_bytes,
     fa_device_status,
     fa_fwd,
     fa_fwd_strided,
+    fa_fwd_varlen,
     library,
     status_string,
 )

@@ -69,6 +69,11 @@ def library(path: str | None = None):
             lib.fa_bwd_strided.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, p64, vp, p64,
                                            vp, p64, i, i, i, i, i, f, vp, sz, vp]
             lib.fa_bwd_strided.restype = i
+            lib.fa_fwd_varlen.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, i, i, i, i, i, i, f, vp]
+            lib.fa_fwd_varlen.restype = i
+            lib.fa_bwd_varlen.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, p64, vp, p64,
+                                          vp, p64, vp, i, i, i, i, i, i, f, vp, sz, vp]
+            lib.fa_bwd_varlen.restype = i
             lib.fa_status_string.argtypes = [i]
             lib.fa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -168,6 +173,88 @@ def fa_bwd_strided(q, k, v, o, dout, lse, causal: bool = False, scale: float | N
                                   _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_strided")
+    return dq, dk, dv
+
+
+def _check_packed(name, t, shape=None):
+    """A [T, H, d] bf16 CUDA view with contiguous d."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 3 or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be a [T, H, d] view with contiguous d")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _strides2(t):
+    return (ctypes.c_int64 * 2)(t.stride(0), t.stride(1))
+
+
+def _check_cu(cu_seqlens):
+    if not isinstance(cu_seqlens, torch.Tensor) or not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 \
+            or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous() or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor of B + 1 row offsets")
+    return cu_seqlens.numel() - 1
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: float | None = None,
+                  o=None, lse=None, stream=None):
+    """Attention over B packed sequences: q, k, v are [T, H, d] (rows of all
+    sequences back to back), sequence b is rows cu_seqlens[b]:cu_seqlens[b+1].
+    Returns (o [T, H, d] bf16, lse [H, T] fp32)."""
+    _check_packed("q", q)
+    T, H, d = q.shape
+    _check_packed("k", k, q.shape)
+    _check_packed("v", v, q.shape)
+    B = _check_cu(cu_seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty(q.shape, device=q.device, dtype=q.dtype) if o is None else o
+    _check_packed("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty((H, T), device=q.device, dtype=torch.float32)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [H, T] tensor")
+    rc = library().fa_fwd_varlen(q.data_ptr(), _strides2(q), k.data_ptr(), _strides2(k), v.data_ptr(), _strides2(v),
+                                 o.data_ptr(), _strides2(o), lse.data_ptr(), cu_seqlens.data_ptr(), B, H, T,
+                                 int(max_seqlen), d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
+    return o, lse
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
+                  scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of fa_fwd_varlen; dq, dk, dv default to contiguous [T, H, d]."""
+    _check_packed("q", q)
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_packed(name, t, q.shape)
+    B = _check_cu(cu_seqlens)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, T) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [H, T]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    new = lambda: torch.empty(q.shape, device=q.device, dtype=q.dtype)  # noqa: E731
+    dq = new() if dq is None else dq
+    dk = new() if dk is None else dk
+    dv = new() if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_packed(name, t, q.shape)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = library().fa_bwd_varlen(q.data_ptr(), _strides2(q), k.data_ptr(), _strides2(k), v.data_ptr(), _strides2(v),
+                                 o.data_ptr(), _strides2(o), dout.data_ptr(), _strides2(dout), lse.data_ptr(),
+                                 dq.data_ptr(), _strides2(dq), dk.data_ptr(), _strides2(dk), dv.data_ptr(),
+                                 _strides2(dv), cu_seqlens.data_ptr(), B, H, T, int(max_seqlen), d,
+                                 int(bool(causal)), float(scale), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
 
 

@@ -112,6 +112,7 @@ bool spans_overlap(uintptr_t alo, uintptr_t ahi, uintptr_t blo, uintptr_t bhi) {
 bool lattice_hit(long long rem, const long long (*dims)[2], int k, int d) {
   if (k == 3) return rem > -d && rem < d;
   const long long st = dims[k][0], ext = dims[k][1];
+  if (ext == 1) return lattice_hit(rem, dims, k + 1, d);  // only a = 0: skip it
   const long long q = rem / st;
   for (long long a = q - 1; a <= q + 1; ++a)
     if (a > -ext && a < ext && lattice_hit(rem - a * st, dims, k + 1, d)) return true;
@@ -191,37 +192,55 @@ const char *fa_status_string(fa_status_t s) {
 namespace fa {
 namespace {
 
+// The row axis of the tensors.  Batched: B slots of N rows each.  Packed
+// (cu != null): one slot of T rows holding the B sequences back to back,
+// N the longest; the tensors' batch stride is then unused (0 in the kernels).
+struct RowAxis {
+  int B, N;
+  const int *cu;
+  int T;
+  int slots() const { return cu ? 1 : B; }
+  int rows() const { return cu ? T : N; }
+};
+
 fa_status_t fwd_impl(const void *q, const Strides &sq, const void *k, const Strides &sk, const void *v,
-                     const Strides &sv, void *o, const Strides &so, float *lse, int B, int H, int N, int d,
+                     const Strides &sv, void *o, const Strides &so, float *lse, const RowAxis &ax, int H, int d,
                      int causal, float scale, cudaStream_t stream) {
+  const int B = ax.B, N = ax.N, SB = ax.slots(), R = ax.rows();
   fa_status_t st = check_common(B, H, N, d, causal, scale);
+  if (st == FA_OK && ax.cu) st = check_common(1, H, R, d, causal, scale);
   if (st != FA_OK) return st;
   const void *ptrs[5] = {q, k, v, o, lse};
   for (const void *x : ptrs)
     if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
-  if (!injective(B, H, N, d, so)) return FA_ERR_INVALID_ARGUMENT;
-  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  if (!injective(SB, H, R, d, so)) return FA_ERR_INVALID_ARGUMENT;
+  const size_t lb = static_cast<size_t>(SB) * H * R * 4;
   uintptr_t olo, ohi, llo = reinterpret_cast<uintptr_t>(lse), lhi = llo + lb;
-  span(o, B, H, N, d, so, &olo, &ohi);
+  span(o, SB, H, R, d, so, &olo, &ohi);
   const void *ins[3] = {q, k, v};
   const Strides *ins_s[3] = {&sq, &sk, &sv};
   for (int i = 0; i < 3; ++i) {
     uintptr_t lo, hi;
-    span(ins[i], B, H, N, d, *ins_s[i], &lo, &hi);
-    if (may_overlap(ins[i], *ins_s[i], o, so, B, H, N, d) || spans_overlap(lo, hi, llo, lhi))
+    span(ins[i], SB, H, R, d, *ins_s[i], &lo, &hi);
+    if (may_overlap(ins[i], *ins_s[i], o, so, SB, H, R, d) || spans_overlap(lo, hi, llo, lhi))
       return FA_ERR_INVALID_ARGUMENT;
   }
   if (spans_overlap(olo, ohi, llo, lhi)) return FA_ERR_INVALID_ARGUMENT;
 
   CUtensorMap tq, tk, tv;
-  if (!encode_map(&tq, q, B, H, N, d, sq) || !encode_map(&tk, k, B, H, N, d, sk) ||
-      !encode_map(&tv, v, B, H, N, d, sv))
+  if (!encode_map(&tq, q, SB, H, R, d, sq) || !encode_map(&tk, k, SB, H, R, d, sk) ||
+      !encode_map(&tv, v, SB, H, R, d, sv))
     return FA_ERR_CUDA;
   FwdParams p{};
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.so = so;
+  if (ax.cu) p.so.b = 0;
   p.H = H;
+  p.cu_seqlens = ax.cu;
+  p.T = R;
+  p.lse_b = ax.cu ? 0 : static_cast<long long>(H) * N;
+  p.lse_h = R;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
@@ -235,9 +254,11 @@ fa_status_t fwd_impl(const void *q, const Strides &sq, const void *k, const Stri
 fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Strides &sk, const void *v,
                      const Strides &sv, const void *o, const Strides &so, const void *dO, const Strides &sdo,
                      const float *lse, void *dq, const Strides &sdq, void *dk, const Strides &sdk, void *dv,
-                     const Strides &sdv, int B, int H, int N, int d, int causal, float scale, void *workspace,
+                     const Strides &sdv, const RowAxis &ax, int H, int d, int causal, float scale, void *workspace,
                      size_t workspace_bytes, cudaStream_t stream) {
+  const int B = ax.B, N = ax.N, SB = ax.slots(), R = ax.rows();
   fa_status_t st = check_common(B, H, N, d, causal, scale);
+  if (st == FA_OK && ax.cu) st = check_common(1, H, R, d, causal, scale);
   if (st != FA_OK) return st;
   const void *ptrs[9] = {q, k, v, o, dO, lse, dq, dk, dv};
   for (const void *x : ptrs)
@@ -245,22 +266,22 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   void *outs[3] = {dq, dk, dv};
   const Strides *outs_s[3] = {&sdq, &sdk, &sdv};
   for (int i = 0; i < 3; ++i)
-    if (!injective(B, H, N, d, *outs_s[i])) return FA_ERR_INVALID_ARGUMENT;
+    if (!injective(SB, H, R, d, *outs_s[i])) return FA_ERR_INVALID_ARGUMENT;
   uintptr_t in_lo[6], in_hi[6], out_lo[3], out_hi[3];
   const void *ins[5] = {q, k, v, o, dO};
   const Strides *ins_s[5] = {&sq, &sk, &sv, &so, &sdo};
-  for (int i = 0; i < 5; ++i) span(ins[i], B, H, N, d, *ins_s[i], &in_lo[i], &in_hi[i]);
+  for (int i = 0; i < 5; ++i) span(ins[i], SB, H, R, d, *ins_s[i], &in_lo[i], &in_hi[i]);
   in_lo[5] = reinterpret_cast<uintptr_t>(lse);
-  in_hi[5] = in_lo[5] + static_cast<size_t>(B) * H * N * 4;
-  for (int i = 0; i < 3; ++i) span(outs[i], B, H, N, d, *outs_s[i], &out_lo[i], &out_hi[i]);
+  in_hi[5] = in_lo[5] + static_cast<size_t>(SB) * H * R * 4;
+  for (int i = 0; i < 3; ++i) span(outs[i], SB, H, R, d, *outs_s[i], &out_lo[i], &out_hi[i]);
   for (int j = 0; j < 3; ++j) {
     for (int i = 0; i < 5; ++i)
-      if (may_overlap(ins[i], *ins_s[i], outs[j], *outs_s[j], B, H, N, d)) return FA_ERR_INVALID_ARGUMENT;
+      if (may_overlap(ins[i], *ins_s[i], outs[j], *outs_s[j], SB, H, R, d)) return FA_ERR_INVALID_ARGUMENT;
     if (spans_overlap(in_lo[5], in_hi[5], out_lo[j], out_hi[j])) return FA_ERR_INVALID_ARGUMENT;  // lse
   }
   for (int i = 0; i < 3; ++i)
     for (int j = i + 1; j < 3; ++j)
-      if (may_overlap(outs[i], *outs_s[i], outs[j], *outs_s[j], B, H, N, d)) return FA_ERR_INVALID_ARGUMENT;
+      if (may_overlap(outs[i], *outs_s[i], outs[j], *outs_s[j], SB, H, R, d)) return FA_ERR_INVALID_ARGUMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (workspace) {
     if (workspace_bytes < need) return FA_ERR_WORKSPACE;
@@ -274,8 +295,8 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
 
   const int BH = B * H;
   CUtensorMap tq, tk, tv, tdo;
-  if (!encode_map(&tq, q, B, H, N, d, sq) || !encode_map(&tk, k, B, H, N, d, sk) ||
-      !encode_map(&tv, v, B, H, N, d, sv) || !encode_map(&tdo, dO, B, H, N, d, sdo))
+  if (!encode_map(&tq, q, SB, H, R, d, sq) || !encode_map(&tk, k, SB, H, R, d, sk) ||
+      !encode_map(&tv, v, SB, H, R, d, sv) || !encode_map(&tdo, dO, SB, H, R, d, sdo))
     return FA_ERR_CUDA;
 
   void *ws = workspace;
@@ -301,7 +322,12 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   p.sdq = sdq;
   p.sdk = sdk;
   p.sdv = sdv;
+  if (ax.cu) p.sq.b = p.so.b = p.sdo.b = p.sdq.b = p.sdk.b = p.sdv.b = 0;
   p.H = H;
+  p.cu_seqlens = ax.cu;
+  p.T = R;
+  p.lse_b = ax.cu ? 0 : static_cast<long long>(H) * N;
+  p.lse_h = R;
   p.status = status_ptr();
   p.N = N;
   p.BH = BH;
@@ -325,7 +351,7 @@ extern "C" {
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
                    int causal, float scale, cudaStream_t stream) {
   const Strides s = contiguous(H, N, d);
-  return fwd_impl(q, s, k, s, v, s, o, s, lse, B, H, N, d, causal, scale, stream);
+  return fwd_impl(q, s, k, s, v, s, o, s, lse, RowAxis{B, N, nullptr, 0}, H, d, causal, scale, stream);
 }
 
 fa_status_t fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
@@ -337,7 +363,7 @@ fa_status_t fa_fwd_strided(const void *q, const int64_t *q_strides, const void *
   if (!normalise(q_strides, B, H, N, d, &sq) || !normalise(k_strides, B, H, N, d, &sk) ||
       !normalise(v_strides, B, H, N, d, &sv) || !normalise(o_strides, B, H, N, d, &so))
     return FA_ERR_INVALID_ARGUMENT;
-  return fwd_impl(q, sq, k, sk, v, sv, o, so, lse, B, H, N, d, causal, scale, stream);
+  return fwd_impl(q, sq, k, sk, v, sv, o, so, lse, RowAxis{B, N, nullptr, 0}, H, d, causal, scale, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -350,8 +376,8 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
                    void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal, float scale, void *workspace,
                    size_t workspace_bytes, cudaStream_t stream) {
   const Strides s = contiguous(H, N, d);
-  return bwd_impl(q, s, k, s, v, s, o, s, dO, s, lse, dq, s, dk, s, dv, s, B, H, N, d, causal, scale, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(q, s, k, s, v, s, o, s, dO, s, lse, dq, s, dk, s, dv, s, RowAxis{B, N, nullptr, 0}, H, d, causal,
+                  scale, workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
@@ -366,8 +392,52 @@ fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const void *
   const int64_t *in[8] = {q_strides, k_strides, v_strides, o_strides, dO_strides, dq_strides, dk_strides, dv_strides};
   for (int i = 0; i < 8; ++i)
     if (!normalise(in[i], B, H, N, d, &s[i])) return FA_ERR_INVALID_ARGUMENT;
-  return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7], B, H, N, d,
-                  causal, scale, workspace, workspace_bytes, stream);
+  return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7],
+                  RowAxis{B, N, nullptr, 0}, H, d, causal, scale, workspace, workspace_bytes, stream);
+}
+
+// Packed sequences: strides arrays of two (row, head); the batch stride of
+// the one slot is derived (never used by the kernels).
+static bool normalise_packed(const int64_t *in, int H, int T, int d, Strides *out) {
+  if (!in) return false;
+  const int64_t full[3] = {0, in[1], in[0]};
+  if (!normalise(full, 1, H, T, d, out)) return false;
+  return true;
+}
+
+fa_status_t fa_fwd_varlen(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                          const void *v, const int64_t *v_strides, void *o, const int64_t *o_strides, float *lse,
+                          const int *cu_seqlens, int B, int H, int T, int max_seqlen, int d, int causal, float scale,
+                          cudaStream_t stream) {
+  fa_status_t st = check_common(B, H, max_seqlen, d, causal, scale);
+  if (st == FA_OK) st = check_common(1, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARGUMENT;
+  Strides sq, sk, sv, so;
+  if (!normalise_packed(q_strides, H, T, d, &sq) || !normalise_packed(k_strides, H, T, d, &sk) ||
+      !normalise_packed(v_strides, H, T, d, &sv) || !normalise_packed(o_strides, H, T, d, &so))
+    return FA_ERR_INVALID_ARGUMENT;
+  return fwd_impl(q, sq, k, sk, v, sv, o, so, lse, RowAxis{B, max_seqlen, cu_seqlens, T}, H, d, causal, scale,
+                  stream);
+}
+
+fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                          const void *v, const int64_t *v_strides, const void *o, const int64_t *o_strides,
+                          const void *dO, const int64_t *dO_strides, const float *lse, void *dq,
+                          const int64_t *dq_strides, void *dk, const int64_t *dk_strides, void *dv,
+                          const int64_t *dv_strides, const int *cu_seqlens, int B, int H, int T, int max_seqlen,
+                          int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  fa_status_t st = check_common(B, H, max_seqlen, d, causal, scale);
+  if (st == FA_OK) st = check_common(1, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARGUMENT;
+  Strides s[8];
+  const int64_t *in[8] = {q_strides, k_strides, v_strides, o_strides, dO_strides, dq_strides, dk_strides, dv_strides};
+  for (int i = 0; i < 8; ++i)
+    if (!normalise_packed(in[i], H, T, d, &s[i])) return FA_ERR_INVALID_ARGUMENT;
+  return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7],
+                  RowAxis{B, max_seqlen, cu_seqlens, T}, H, d, causal, scale, workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_device_status(cudaStream_t stream) {

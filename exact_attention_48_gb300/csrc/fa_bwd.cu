@@ -61,13 +61,14 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   const bool in_range = prow < static_cast<long long>(p.BH) * Np;
   const int bh = in_range ? static_cast<int>(prow / Np) : 0;
   const int q = in_range ? static_cast<int>(prow % Np) : 0;
-  const bool real = in_range && q < p.N;
-  const long long row = static_cast<long long>(bh) * p.N + q;
+  const SeqRange seq = seq_range(p.cu_seqlens, bh / p.H, p.N, p.T);
+  const bool real = in_range && q < seq.len;
+  const int trow = seq.start + q;  // the row on the tensors' row axis
   const int part = threadIdx.x % kTpr;
   float acc = 0.0f;
   if (real) {
-    const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row_offset(p.so, bh, p.H, q))[part];
-    const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row_offset(p.sdo, bh, p.H, q))[part];
+    const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row_offset(p.so, bh, p.H, trow))[part];
+    const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row_offset(p.sdo, bh, p.H, trow))[part];
     const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
     const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
 #pragma unroll
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (in_range && part == 0) {
     p.delta[prow] = acc;
-    p.lse2[prow] = real ? p.lse[row] * kLog2e : INFINITY;
+    p.lse2[prow] = real ? p.lse[(bh / p.H) * p.lse_b + (bh % p.H) * p.lse_h + trow] * kLog2e : INFINITY;
   }
 }
 
@@ -146,7 +147,7 @@ struct BwdLayout {
 // so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
 // dV(t+1) and S^T(t+2) run.  Each product that overwrites a TMEM region
 // comes after the one that reads it (the tensor core runs them in order).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -173,8 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int nblk = p.num_blk;
+  const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
   // Tile order: causal puts the key blocks with the most query blocks
   // (j small) first; otherwise the key blocks of one head run together.
@@ -186,8 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = static_cast<int>(blockIdx.x) / nblk;
     jblk = static_cast<int>(blockIdx.x) % nblk;
   }
-  // Query blocks visited: causal i = j .. nblk-1; otherwise all of them.
-  const int n_q = CAUSAL ? (nblk - jblk) : nblk;
+  // The block's sequence; a block past its end (packed mode) has no work.
+  const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
+  if (VARLEN && jblk * kBlk >= seq.len) return;
+  const int N = seq.len, row0 = seq.start;
+  const int tma_h = bh % p.H, tma_b = VARLEN ? 0 : bh / p.H;
+  const int nb = (N + kBlk - 1) / kBlk;  // blocks of this sequence
+  // Query blocks visited: causal i = j .. nb-1; otherwise all of them.
+  const int n_q = CAUSAL ? (nb - jblk) : nb;
   const int i0 = CAUSAL ? jblk : 0;
 
   if (threadIdx.x == 0) {
@@ -230,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
 #pragma unroll
       for (int s = 0; s < L::kSlabs; ++s) {
-        tma_load_4d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, jblk * kBlk, bh % p.H, bh / p.H);
-        tma_load_4d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, jblk * kBlk, bh % p.H, bh / p.H);
+        tma_load_4d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, row0 + jblk * kBlk, tma_h, tma_b);
+        tma_load_4d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, row0 + jblk * kBlk, tma_h, tma_b);
       }
       int issued = 0;
       for (int t = 0; t < n_q; ++t) {
@@ -241,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + t;
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s) {
-          tma_load_4d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, i * kBlk, bh % p.H,
-                      bh / p.H);
-          tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, i * kBlk, bh % p.H,
-                      bh / p.H);
+          tma_load_4d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
+                      tma_b);
+          tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
+                      tma_b);
         }
         const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + static_cast<size_t>(i) * kBlk;
         bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
@@ -447,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       if (half == 0)
-        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row_offset(p.sdv, bh, p.H, key), key_ok, 1.0f);
+        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row_offset(p.sdv, bh, p.H, row0 + key), key_ok, 1.0f);
       else
-        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row_offset(p.sdk, bh, p.H, key), key_ok, p.scale);
+        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row_offset(p.sdk, bh, p.H, row0 + key), key_ok,
+                         p.scale);
     }
   }
 
@@ -491,7 +498,7 @@ struct DqLayout {
 // S(j+2) runs; dP(j+1) overwrites dS(j) after dQ(j) has read it (the tensor
 // core runs the products in order).  K(j) is read by S(j) and, last, by
 // dQ(j); the third K stage lets K(j+2) load while dQ(j) still holds K(j).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -521,8 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int nblk = p.num_blk;
+  const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
   // Tile order: causal puts the query blocks with the most key blocks
   // (i large) first; otherwise the query blocks of one head run together.
@@ -534,7 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = static_cast<int>(blockIdx.x) / nblk;
     iblk = static_cast<int>(blockIdx.x) % nblk;
   }
-  const int n_kv = CAUSAL ? (iblk + 1) : nblk;  // key blocks 0 .. n_kv-1
+  // The block's sequence; a block past its end (packed mode) has no work.
+  const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
+  if (VARLEN && iblk * kBlk >= seq.len) return;
+  const int N = seq.len, row0 = seq.start;
+  const int tma_h = bh % p.H, tma_b = VARLEN ? 0 : bh / p.H;
+  const int nb = (N + kBlk - 1) / kBlk;                  // blocks of this sequence
+  const int n_kv = CAUSAL ? (iblk + 1) : nb;  // key blocks 0 .. n_kv-1
 
   if (threadIdx.x == 0) {
     mbar_init(do_ready, kRowWarps);
@@ -579,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], L::kTile);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, j * kBlk, bh % p.H, bh / p.H);
+          tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
         issued = j + 1;
       }
       if (*abort_flag)
@@ -594,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&v_full[st], L::kTile);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, j * kBlk, bh % p.H, bh / p.H);
+          tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
         issued = j + 1;
       }
       if (*abort_flag)
@@ -694,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(m ? p.dout + row_offset(p.sdo, bh, p.H, qrow)
-                                                             : p.q + row_offset(p.sq, bh, p.H, qrow));
+        const uint4 *src = reinterpret_cast<const uint4 *>(m ? p.dout + row_offset(p.sdo, bh, p.H, row0 + qrow)
+                                                             : p.q + row_offset(p.sq, bh, p.H, row0 + qrow));
         const uint32_t col = m ? kColDO : kColQ;
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh) {
@@ -719,6 +731,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < n_kv; ++j) {
       const bool diag = CAUSAL && (j == iblk);
+      // packed mode: keys past the sequence are the next sequence's rows and
+      // must get P = 0 (batched mode: they are zero rows of K and V, whose
+      // dS K adds nothing)
+      const int klim = N - 1 - j * kBlk;  // last key column of this block inside the sequence
+      const bool kmask = VARLEN && klim < kBlk - 1;
       // Phase 1: P = exp2(S c - lse2) for this half of the keys, kept as bf16 pairs.
       ok = mbar_wait(s_full, j & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -741,9 +758,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
           float p0 = ex2(x.x), p1 = ex2(x.y);
-          if (diag) {  // key kc visible to query r iff kc <= r
-            p0 = (c0 + ch * 32 + e <= r) ? p0 : 0.0f;
-            p1 = (c0 + ch * 32 + e + 1 <= r) ? p1 : 0.0f;
+          if (diag || kmask) {  // key kc visible to query r iff kc <= r (causal) and kc < N
+            const int lim = diag ? min(r, klim) : klim;
+            p0 = (c0 + ch * 32 + e <= lim) ? p0 : 0.0f;
+            p1 = (c0 + ch * 32 + e + 1 <= lim) ? p1 : 0.0f;
           }
           pf[ch * 16 + e / 2] = make_float2(p0, p1);
         }
@@ -787,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       store_acc_row<D / 2>(tmem + kColDQ + lane_base + half * (D / 2),
-                           p.dq + row_offset(p.sdq, bh, p.H, qrow) + half * (D / 2), qrow < N, p.scale);
+                           p.dq + row_offset(p.sdq, bh, p.H, row0 + qrow) + half * (D / 2), qrow < N, p.scale);
     }
   }
 
@@ -808,7 +826,7 @@ cudaError_t launch_main(Kern kern, unsigned grid, uint32_t smem, const CUtensorM
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                          const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
   using L = BwdLayout<D>;
@@ -820,10 +838,10 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
+  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL>, grid, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo, p, stream);
+  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
   return cudaSuccess;
@@ -833,11 +851,21 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
-  if (d == 64)
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream, ev)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream, ev);
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream, ev)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream, ev);
+  // (the packed-sequence mode is a template parameter: the batched kernels
+  // carry none of its per-block work)
+  const bool v = p.cu_seqlens != nullptr;
+  if (d == 64) {
+    if (causal)
+      return v ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, stream, ev)
+               : launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, stream, ev);
+    return v ? launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, stream, ev)
+             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, stream, ev);
+  }
+  if (causal)
+    return v ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, stream, ev)
+             : launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, stream, ev);
+  return v ? launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, stream, ev)
+           : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, stream, ev);
 }
 
 }  // namespace fa

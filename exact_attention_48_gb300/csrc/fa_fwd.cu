@@ -77,17 +77,21 @@ struct SoftmaxArgs {
   uint32_t tS, tO;  // TMEM columns of this tile's S and O (lane base added inside)
   int n_kv;         // key blocks this tile visits
   int diag;         // causal: index of the diagonal key block, else -1
-  int grow0;        // first query row of the tile
+  int grow0;        // first query row of the tile (within its sequence)
+  int N;            // rows of this tile's sequence
+  int row0;         // first row of the sequence on the tensors' row axis
 };
 
 // Online softmax of one 128-row tile: one query row per thread.
-template <int D>
+template <int D, bool VARLEN>
 __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdParams &p, const WaitCtl &ctl, int bh,
                                              int warp, int lane) {
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const int N = p.N;
+  // batched: the length from the kernel parameters (a constant operand;
+  // measurably faster in this loop than a register copy)
+  const int N = VARLEN ? a.N : p.N;
   const float c = p.scale_log2;
   const bool neg = p.neg != 0;
   const uint32_t tS = a.tS + lane_base, tO = a.tO + lane_base;
@@ -232,7 +236,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     const float inv_l = 1.0f / lb_run;
     const int grow_row = a.grow0 + row;
     const bool store = grow_row < N;
-    __nv_bfloat16 *orow = p.o + row_offset(p.so, bh, p.H, grow_row);
+    __nv_bfloat16 *orow = p.o + row_offset(p.so, bh, p.H, a.row0 + grow_row);
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t o[32];
@@ -248,11 +252,12 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
-    if (store) p.lse[static_cast<size_t>(bh) * N + grow_row] = (m_run + log2f(l_run)) * kLn2;
+    if (store)
+      p.lse[(bh / p.H) * p.lse_b + (bh % p.H) * p.lse_h + a.row0 + grow_row] = (m_run + log2f(l_run)) * kLn2;
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -289,8 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = static_cast<int>(blockIdx.x) / p.num_qblk;
     qb = static_cast<int>(blockIdx.x) % p.num_qblk;
   }
-  const int bh_b = bh / p.H, bh_h = bh % p.H;  // batch and head of the tile (TMA coordinates)
-  const int N = p.N;
+  // The tile's sequence; a tile past its end (packed mode) has no work.
+  const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
+  if (VARLEN && qb * 2 * kBM >= seq.len) return;
+  const int row0 = seq.start;
+  const int bh_h = bh % p.H, bh_b = VARLEN ? 0 : bh / p.H;  // TMA coordinates of the head
+  const int N = seq.len;
   const int nkv_all = (N + kBN - 1) / kBN;
   const int n0 = CAUSAL ? min(2 * qb + 1, nkv_all) : nkv_all;  // key blocks of tile 0
   const int n1 = CAUSAL ? min(2 * qb + 2, nkv_all) : nkv_all;  // key blocks of tile 1 (>= n0)
@@ -338,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, qb * 2 * kBM + t * kBM, bh_h, bh_b);
+          tma_load_4d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, row0 + qb * 2 * kBM + t * kBM, bh_h,
+                      bh_b);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
@@ -347,13 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, j * kBN, bh_h, bh_b);
+          tma_load_4d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBN, bh_h, bh_b);
         k_issued = j + 1;
         if (!mbar_wait(&v_empty[st], ph ^ 1, ctl, kSiteVEmpty)) break;
         mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, j * kBN, bh_h, bh_b);
+          tma_load_4d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBN, bh_h, bh_b);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -443,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     a.n_kv = t ? n1 : n0;
     a.diag = CAUSAL ? 2 * qb + t : -1;
     a.grow0 = qb * 2 * kBM + t * kBM;
-    softmax_tile<D>(a, p, ctl, bh, warp, lane);
+    a.N = N;
+    a.row0 = row0;
+    softmax_tile<D, VARLEN>(a, p, ctl, bh, warp, lane);
   }
 
   tc_fence_before();
@@ -454,11 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const FwdParams &p,
                          cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_qblk);
@@ -470,8 +482,15 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, cudaStream_t stream) {
-  if (d == 64) return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, stream) : launch_fwd_t<64, false>(tq, tk, tv, p, stream);
-  return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, stream) : launch_fwd_t<128, false>(tq, tk, tv, p, stream);
+  // (the packed-sequence mode is a template parameter: the batched kernels
+  // carry none of its per-tile work)
+  const bool v = p.cu_seqlens != nullptr;
+  if (d == 64) {
+    if (causal) return v ? launch_fwd_t<64, true, true>(tq, tk, tv, p, stream) : launch_fwd_t<64, true, false>(tq, tk, tv, p, stream);
+    return v ? launch_fwd_t<64, false, true>(tq, tk, tv, p, stream) : launch_fwd_t<64, false, false>(tq, tk, tv, p, stream);
+  }
+  if (causal) return v ? launch_fwd_t<128, true, true>(tq, tk, tv, p, stream) : launch_fwd_t<128, true, false>(tq, tk, tv, p, stream);
+  return v ? launch_fwd_t<128, false, true>(tq, tk, tv, p, stream) : launch_fwd_t<128, false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace fa

@@ -39,11 +39,32 @@ __host__ __device__ inline long long row_offset(const Strides &s, int bh, int H,
   return static_cast<long long>(bh / H) * s.b + static_cast<long long>(bh % H) * s.h + static_cast<long long>(n) * s.n;
 }
 
+// Rows of the sequence of batch entry b: [start, start + len) of the
+// tensors' row axis.  Batched mode (cu == null): every sequence is rows
+// [0, N) of its own batch slot.  Packed ("varlen") mode: sequence b is rows
+// [cu[b], cu[b+1]) of one packed row axis of T rows, N is the longest
+// sequence; the bounds are clamped into [0, T] and the length to N, so that
+// no access leaves the tensors whatever the array holds.
+struct SeqRange {
+  int start, len;
+};
+__device__ inline SeqRange seq_range(const int *cu, int b, int N, int T) {
+  if (!cu) return SeqRange{0, N};
+  int s = cu[b], e = cu[b + 1];
+  s = s < 0 ? 0 : (s > T ? T : s);
+  e = e < s ? s : (e > T ? T : e);
+  const int len = e - s;
+  return SeqRange{s, len < N ? len : N};
+}
+
 struct FwdParams {
   __nv_bfloat16 *o;   // [B, H, N, d] with strides so
   float *lse;         // [BH, N] contiguous
   Strides so;
   int H;
+  const int *cu_seqlens;       // packed mode: B+1 row offsets (device); null in batched mode
+  int T;                       // packed mode: rows of the packed row axis
+  long long lse_b, lse_h;      // lse index = b*lse_b + h*lse_h + row (row on the tensors' row axis)
   int *status;        // device status block (2 ints)
   int N;
   int BH;
@@ -64,6 +85,9 @@ struct BwdParams {
   __nv_bfloat16 *dv;
   Strides sq, so, sdo, sdq, sdk, sdv;
   int H;
+  const int *cu_seqlens;       // as in FwdParams
+  int T;
+  long long lse_b, lse_h;
   int *status;
   int N;
   int BH;

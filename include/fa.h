@@ -138,6 +138,46 @@ FA_API fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const
                                   cudaStream_t stream);
 
 /*
+ * Packed variable-length sequences ("varlen").  B sequences of different
+ * lengths stored back to back along one row axis of T rows: sequence b is
+ * rows [cu_seqlens[b], cu_seqlens[b+1]) of every tensor, and attends only
+ * to itself (causal = 1: key j visible to query i iff j <= i, positions
+ * counted from the sequence's first row).
+ *   q, k, v, o, dO, dq, dk, dv : [T, H, d] bf16 with element strides
+ *                    strides[0] between rows and strides[1] between heads
+ *                    (d contiguous; same rules as the strided calls)
+ *   lse          : [H, T] fp32, contiguous
+ *   cu_seqlens   : device array of B + 1 int32 row offsets, 4-byte aligned:
+ *                  0 = cu[0] <= cu[1] <= ... <= cu[B] = T, every length
+ *                  cu[b+1] - cu[b] at most max_seqlen.  The kernels read it
+ *                  on the device, so the host cannot check it; they clamp
+ *                  every offset into [0, T] and every length to max_seqlen,
+ *                  so a malformed array gives wrong results for the
+ *                  sequences it describes, never an access outside the
+ *                  tensors.  Zero-length sequences are allowed.
+ *   max_seqlen   : the longest sequence (sizes the launch and the workspace)
+ * The backward workspace is fa_bwd_workspace_bytes(B, H, max_seqlen, d).
+ * The pages describe attention per sequence; packing several sequences into
+ * one call is this library's reading of the framework integration that the
+ * page "FlashAttention-2 (DE)", section "Anwendung und Integration in das
+ * Oekosystem", names.
+ */
+FA_API fa_status_t fa_fwd_varlen(const void *q, const int64_t *q_strides, const void *k,
+                                 const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                                 void *o, const int64_t *o_strides, float *lse,
+                                 const int *cu_seqlens, int B, int H, int T, int max_seqlen, int d,
+                                 int causal, float scale, cudaStream_t stream);
+
+FA_API fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const void *k,
+                                 const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                                 const void *o, const int64_t *o_strides, const void *dO,
+                                 const int64_t *dO_strides, const float *lse, void *dq,
+                                 const int64_t *dq_strides, void *dk, const int64_t *dk_strides,
+                                 void *dv, const int64_t *dv_strides, const int *cu_seqlens, int B,
+                                 int H, int T, int max_seqlen, int d, int causal, float scale,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Size in bytes of the fixed device array that fa_bwd_noalloc uses as its
  * scratch (8 MiB).  Every GPU that loads the library holds this array until
  * the process exits.  It covers B * H * Np <= 1,048,576 padded rows, where

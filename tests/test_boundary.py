@@ -152,3 +152,20 @@ def test_bwd_strided_rejects(lib):
     # after dq collides with dq's second head (a gap of H*d would not)
     packed = _s(N * 3 * H * d, d, 3 * H * d)
     assert call(dqs=packed, dk=FAKE + (10 << 30) + 2 * d, dks=packed) == FA_ERR_INVALID_ARGUMENT
+
+
+def test_varlen_rejects(lib):
+    H, T, d = 2, 300, 64
+    c = (ctypes.c_int64 * 2)(H * d, d)
+
+    def fwd(cu=FAKE + (6 << 30), qs=c, B=3, maxlen=200, o=FAKE + (3 << 30)):
+        return lib.fa_fwd_varlen(FAKE, qs, FAKE + (1 << 30), c, FAKE + (2 << 30), c, o, c, FAKE + (4 << 30), cu,
+                                 B, H, T, maxlen, d, 1, 0.125, None)
+    assert fwd(cu=None) == FA_ERR_INVALID_ARGUMENT
+    assert fwd(cu=FAKE + (6 << 30) + 2) == FA_ERR_INVALID_ARGUMENT                        # misaligned offsets
+    assert fwd(B=0) == FA_ERR_INVALID_ARGUMENT
+    assert fwd(maxlen=0) == FA_ERR_INVALID_ARGUMENT
+    assert fwd(qs=(ctypes.c_int64 * 2)(H * d + 4, d)) == FA_ERR_INVALID_ARGUMENT          # row stride not x8
+    assert fwd(o=FAKE + (2 << 30) + 1024) == FA_ERR_INVALID_ARGUMENT                     # o inside v
+    assert lib.fa_bwd_varlen(FAKE, c, FAKE, c, FAKE, c, FAKE, c, FAKE, c, FAKE, FAKE, c, FAKE, c, FAKE, c, None,
+                             3, H, T, 200, d, 0, 0.125, None, 0, None) == FA_ERR_INVALID_ARGUMENT
