@@ -44,7 +44,8 @@ def parse_args():
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--workload", choices=["sweep", "fwd_b8h16n2048d64", "causal_b4h32n4096d128",
-                                           "long_b1h16n16384d128x2"], default="sweep",
+                                           "long_b1h16n16384d128x2", "bnhd_b2h16n8192d128",
+                                           "varlen_t16384h16d128_causal"], default="sweep",
                     help="a named workload instead of the sweep point given by --N/--d/--causal "
                          "(the forward-only one times the forward alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -57,7 +58,9 @@ def parse_args():
 def workload(args):
     from exact_attention_48_gb300 import inputs
     named = {"fwd_b8h16n2048d64": inputs.FWD_B8H16N2048D64, "causal_b4h32n4096d128": inputs.CAUSAL_B4H32N4096D128,
-             "long_b1h16n16384d128x2": inputs.LONG_B1H16N16384D128}
+             "long_b1h16n16384d128x2": inputs.LONG_B1H16N16384D128,
+             "bnhd_b2h16n8192d128": inputs.BNHD_B2H16N8192D128,
+             "varlen_t16384h16d128_causal": inputs.VARLEN_T16384H16D128}
     if getattr(args, "workload", "sweep") != "sweep":
         return named[args.workload]
     return inputs.sweep(args.N, args.d, args.causal)
@@ -226,9 +229,14 @@ def aggregate_throughput(flops_per_step_per_rank: float, steps: int, local_ms: f
 
 # ------------------------------------------------------------------ GPU
 
+def token_rows(w):
+    """Rows of one head over the whole batch (B*N, or the packed total)."""
+    return sum(w.lengths) if w.layout == "varlen" else w.B * w.N
+
+
 def touched_bytes(w):
     n_t = 8 if w.backward else 4  # q, k, v, o (+ dO, dQ, dK, dV)
-    return n_t * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.N * 4
+    return n_t * token_rows(w) * w.H * w.d * 2 + token_rows(w) * w.H * 4
 
 
 def needs_flush(w):
@@ -241,11 +249,78 @@ def config_of(w):
           if not needs_flush(w) else
           f"L2 flushed between steps (a 256 MiB write); the tensors touched per step ({touched / 2**20:.0f} MiB) "
           f"would fit in L2; value = work / sum of the per-step CUDA-event times")
-    return {"workload": f"{'fwd+bwd' if w.backward else 'fwd'} B{w.B} H{w.H} N{w.N} d{w.d} "
-                        f"{'causal' if w.causal else 'non-causal'} bf16",
-            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
-            "inputs": f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}",
-            "l2": l2}
+    shape = f"B{w.B} H{w.H} N{w.N} d{w.d}"
+    if w.layout == "bnhd":
+        shape += " stored [B, N, H, d]"
+    elif w.layout == "varlen":
+        shape = f"T{token_rows(w)} ({w.B} packed sequences, longest {w.N}) H{w.H} d{w.d}"
+    c = {"workload": f"{'fwd+bwd' if w.backward else 'fwd'} {shape} "
+                     f"{'causal' if w.causal else 'non-causal'} bf16",
+         "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
+         "layout": w.layout,
+         "inputs": f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}",
+         "l2": l2}
+    if w.layout == "varlen":
+        c["lengths"] = list(w.lengths)
+    return c
+
+
+class Problem:
+    """Device tensors of one workload in its storage layout, and the calls
+    of the public API that run the path on them.
+
+    ``inputs`` (q, k, v, dO) and ``outputs`` (o, dq, dk, dv) are the storage
+    tensors (what a caller copies); ``fwd``/``bwd`` take storage tensors and
+    hand the API the views it expects."""
+
+    def __init__(self, w, device="cuda"):
+        import torch
+        import exact_attention_48_gb300 as fa
+        from exact_attention_48_gb300.inputs import draw, draw_shape
+        self.w = w
+        if w.layout == "varlen":
+            T = token_rows(w)
+            q, k, v, do = draw_shape(1, w.H, T, w.d, w.seed, w.input_mult, device)
+            self.inputs = [x[0].transpose(0, 1).contiguous() for x in (q, k, v, do)]  # [T, H, d]
+            offs = [0]
+            for n in w.lengths:
+                offs.append(offs[-1] + n)
+            self.cu = torch.tensor(offs, dtype=torch.int32, device=device)
+            self.lse_shape = (w.H, T)
+        else:
+            q, k, v, do = draw(w, device=device)
+            if w.layout == "bnhd":
+                self.inputs = [x.transpose(1, 2).contiguous() for x in (q, k, v, do)]  # [B, N, H, d]
+            else:
+                self.inputs = [q, k, v, do]
+            self.lse_shape = (w.B, w.H, w.N)
+        self.outputs = [torch.empty_like(self.inputs[0]) for _ in range(4)]
+        self.lse = torch.empty(self.lse_shape, device=device, dtype=torch.float32)
+        self.ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=device, dtype=torch.uint8)
+        self._fa = fa
+
+    def view(self, x):
+        return x.transpose(1, 2) if self.w.layout == "bnhd" else x
+
+    def fwd(self, q, k, v, o, lse):
+        w, fa, V = self.w, self._fa, self.view
+        if w.layout == "varlen":
+            fa.fa_fwd_varlen(q, k, v, self.cu, w.N, w.causal, w.scale, o=o, lse=lse)
+        elif w.layout == "bnhd":
+            fa.fa_fwd_strided(V(q), V(k), V(v), w.causal, w.scale, o=V(o), lse=lse)
+        else:
+            fa.fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
+
+    def bwd(self, q, k, v, o, do, lse, dq, dk, dv):
+        w, fa, V = self.w, self._fa, self.view
+        if w.layout == "varlen":
+            fa.fa_bwd_varlen(q, k, v, o, do, lse, self.cu, w.N, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+                             workspace=self.ws)
+        elif w.layout == "bnhd":
+            fa.fa_bwd_strided(V(q), V(k), V(v), V(o), V(do), lse, w.causal, w.scale, dq=V(dq), dk=V(dk),
+                              dv=V(dv), workspace=self.ws)
+        else:
+            fa.fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=self.ws)
 
 
 def traffic_record(kernel: str, workload_name: str):
@@ -282,17 +357,15 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    from exact_attention_48_gb300 import fa_bwd, fa_bwd_workspace_bytes, fa_device_status, fa_fwd
+    from exact_attention_48_gb300 import fa_device_status
     from exact_attention_48_gb300.binding import fa_debug_time_next_bwd
-    from exact_attention_48_gb300.inputs import draw
 
     w = workload(args)
     # every rank runs its own batch (independent heads): weak scaling, no data-path collective
-    q, k, v, do = draw(w, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), device="cuda", dtype=torch.float32)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws = torch.empty(fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
+    pb = Problem(w)
+    q, k, v, do = pb.inputs
+    o, dq, dk, dv = pb.outputs
+    lse = pb.lse
     stream = torch.cuda.current_stream()
 
     bwd_on = w.backward  # the forward-only workload times the forward alone
@@ -300,13 +373,13 @@ def run_ours(args):
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
+        pb.fwd(q, k, v, o, lse)
         if evs is not None:
             evs[1].record(stream)
         if bwd_on:
             if evs is not None:
                 fa_debug_time_next_bwd(evs[2], evs[3], evs[4])
-            fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+            pb.bwd(q, k, v, o, do, lse, dq, dk, dv)
         if evs is not None:
             evs[5].record(stream)
 
@@ -390,7 +463,7 @@ def run_ours(args):
     }
 
     if not args.no_e2e:
-        line["e2e"] = e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world)
+        line["e2e"] = e2e_leg(pb, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -400,18 +473,20 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
+def e2e_leg(pb, args, world):
     """Same metric through the public API from HOST buffers: every step copies
     q, k, v, dO from pinned host memory to the device and o, lse, dq, dk, dv
     back, inside the timed region."""
     import torch
-    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+    w = pb.w
+    q = pb.inputs[0]
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in pb.inputs)
     outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4)]
-    hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    hlse = torch.empty(pb.lse_shape, dtype=torch.float32).pin_memory()
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     q_, k_, v_, do_ = (torch.empty_like(q) for _ in range(4))
     o_ = torch.empty_like(q)
-    lse_ = torch.empty((w.B, w.H, w.N), device="cuda", dtype=torch.float32)
+    lse_ = torch.empty(pb.lse_shape, device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 20))
     n_in, n_out = (4, 4) if w.backward else (3, 1)
@@ -419,9 +494,9 @@ def e2e_leg(w, args, q, k, v, do, fa_fwd, fa_bwd, ws, world):
     def step():
         for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo))[:n_in]:
             dst.copy_(src, non_blocking=True)
-        fa_fwd(q_, k_, v_, w.causal, w.scale, o=o_, lse=lse_)
+        pb.fwd(q_, k_, v_, o_, lse_)
         if w.backward:
-            fa_bwd(q_, k_, v_, o_, do_, lse_, w.causal, w.scale, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
+            pb.bwd(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_)
         for dst, src in zip(outs, (o_, dq_, dk_, dv_)[:n_out]):
             dst.copy_(src, non_blocking=True)
         hlse.copy_(lse_, non_blocking=True)

@@ -29,13 +29,18 @@ class Workload:
     input_mult: float = 1.0   # Q/K/V are N(0,1) * input_mult (dO stays N(0,1))
     seed: int = 1000
     note: str = field(default="", compare=False)
+    layout: str = "bhnd"      # "bhnd" contiguous, "bnhd" ([B, N, H, d] storage), "varlen" (packed sequences)
+    lengths: tuple = ()       # varlen: the B sequence lengths (N is the longest)
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
     def flops_fwd(self) -> float:
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        if self.layout == "varlen":
+            f = sum(4.0 * self.H * n * n * self.d for n in self.lengths)
+        else:
+            f = 4.0 * self.B * self.H * self.N * self.N * self.d
         return f / 2 if self.causal else f
 
     def flops_bwd(self) -> float:
@@ -60,6 +65,29 @@ def sweep(N: int, d: int, causal: bool) -> Workload:
     return Workload(f"sweep_b{B}h16n{N}d{d}{'_causal' if causal else ''}", B, 16, N, d, causal,
                     True, 1.0, 1004 + N * 10 + d)
 
+
+def varlen_lengths(total: int, lo: int, hi: int, seed: int) -> tuple:
+    """Seeded sequence lengths in [lo, hi] adding up to ``total`` (the last
+    one takes the remainder, at least 1)."""
+    g = torch.Generator()
+    g.manual_seed(int(seed))
+    out, left = [], total
+    while left > hi:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        out.append(n)
+        left -= n
+    out.append(left)
+    return tuple(out)
+
+
+# The strided and packed paths measured on training-like shapes: the
+# headline shape stored [B, N, H, d], and 16384 tokens of sequences of
+# 256..4096 tokens packed back to back (causal, as in packed LM training).
+BNHD_B2H16N8192D128 = Workload("bnhd_b2h16n8192d128", 2, 16, 8192, 128, False, True, 1.0, 1005,
+                               "headline shape, [B, N, H, d] storage", layout="bnhd")
+_VL = varlen_lengths(16384, 256, 4096, 1006)
+VARLEN_T16384H16D128 = Workload("varlen_t16384h16d128_causal", len(_VL), 16, max(_VL), 128, True, True, 1.0,
+                                1006, "packed sequences of 256..4096 tokens", layout="varlen", lengths=_VL)
 
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
 HEADLINE = sweep(8192, 128, False)   # B=2, H=16, N=8192, d=128, non-causal

@@ -104,3 +104,62 @@ def test_sweep_points_d128(N, causal):
 @pytest.mark.parametrize("N", [512, 4096])
 def test_sweep_points_d64(N):
     _run(sweep(N, 64, True), heads_max=2)
+
+
+def _bench_problem(w):
+    import bench
+    pb = bench.Problem(w)
+    q, k, v, do = pb.inputs
+    o, dq, dk, dv = pb.outputs
+    pb.fwd(q, k, v, o, pb.lse)
+    pb.bwd(q, k, v, o, do, pb.lse, dq, dk, dv)
+    assert fa_device_status() == 0
+    torch.cuda.synchronize()
+    return pb
+
+
+def test_bnhd_b2h16n8192d128():
+    """The headline shape stored [B, N, H, d], through the strided calls as
+    bench.py drives them: sampled heads against the oracle, every head of O
+    against the contiguous path bit for bit."""
+    from exact_attention_48_gb300.inputs import BNHD_B2H16N8192D128 as w
+    pb = _bench_problem(w)
+    q, k, v, do = (x.transpose(1, 2) for x in pb.inputs)   # [B, H, N, d] views
+    o, dq, dk, dv = (x.transpose(1, 2) for x in pb.outputs)
+    for hh in heads_to_check(w.B, w.H, max_heads=2):
+        b, h = divmod(hh, w.H)
+        o_ref, lse_ref = oracle.fwd(q[b, h], k[b, h], v[b, h], w.causal, w.scale)
+        spread = oracle.fwd_spread(q[b, h], k[b, h], v[b, h], w.causal, w.scale)
+        check_o(o[b, h], o_ref, f"{w.name} head {hh}", spread)
+        check_lse(pb.lse[b, h], lse_ref, f"{w.name} head {hh}")
+        refs = oracle.bwd(q[b, h], k[b, h], v[b, h], do[b, h], w.causal, w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            check_grad(g, r, name, f"{w.name} head {hh}")
+    oc, lc = fa_fwd(q.contiguous(), k.contiguous(), v.contiguous(), w.causal, w.scale)
+    assert torch.equal(oc, o) and torch.equal(lc, pb.lse)
+
+
+def test_varlen_t16384h16d128_causal():
+    """16384 packed tokens of 7 sequences, causal, as bench.py drives them:
+    the first, the longest and the last sequence against the oracle (one
+    head each), and every output row finite."""
+    from exact_attention_48_gb300.inputs import VARLEN_T16384H16D128 as w
+    pb = _bench_problem(w)
+    q, k, v, do = pb.inputs                                  # [T, H, d]
+    o, dq, dk, dv = pb.outputs
+    offs = [0]
+    for n in w.lengths:
+        offs.append(offs[-1] + n)
+    longest = max(range(w.B), key=lambda i: w.lengths[i])
+    for b, h in ((0, 0), (longest, w.H // 2), (w.B - 1, w.H - 1)):
+        r0, r1 = offs[b], offs[b + 1]
+        sl = lambda x: x[r0:r1, h]  # noqa: E731
+        o_ref, lse_ref = oracle.fwd(sl(q), sl(k), sl(v), w.causal, w.scale)
+        spread = oracle.fwd_spread(sl(q), sl(k), sl(v), w.causal, w.scale)
+        check_o(sl(o), o_ref, f"{w.name} seq {b} head {h}", spread)
+        check_lse(pb.lse[h, r0:r1], lse_ref, f"{w.name} seq {b} head {h}")
+        refs = oracle.bwd(sl(q), sl(k), sl(v), sl(do), w.causal, w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (sl(dq), sl(dk), sl(dv)), refs):
+            check_grad(g, r, name, f"{w.name} seq {b} head {h}")
+    for t in (o, dq, dk, dv):
+        assert bool(torch.isfinite(t.float()).all())
