@@ -45,7 +45,8 @@ def parse_args():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--workload", choices=["sweep", "fwd_b8h16n2048d64", "causal_b4h32n4096d128",
                                            "long_b1h16n16384d128x2", "bnhd_b2h16n8192d128",
-                                           "varlen_t16384h16d128_causal"], default="sweep",
+                                           "varlen_t16384h16d128_causal", "decode_b16h16nk16384d128"],
+                    default="sweep",
                     help="a named workload instead of the sweep point given by --N/--d/--causal "
                          "(the forward-only one times the forward alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -60,7 +61,8 @@ def workload(args):
     named = {"fwd_b8h16n2048d64": inputs.FWD_B8H16N2048D64, "causal_b4h32n4096d128": inputs.CAUSAL_B4H32N4096D128,
              "long_b1h16n16384d128x2": inputs.LONG_B1H16N16384D128,
              "bnhd_b2h16n8192d128": inputs.BNHD_B2H16N8192D128,
-             "varlen_t16384h16d128_causal": inputs.VARLEN_T16384H16D128}
+             "varlen_t16384h16d128_causal": inputs.VARLEN_T16384H16D128,
+             "decode_b16h16nk16384d128": inputs.DECODE_B16H16NK16384D128}
     if getattr(args, "workload", "sweep") != "sweep":
         return named[args.workload]
     return inputs.sweep(args.N, args.d, args.causal)
@@ -166,7 +168,35 @@ def oracle_sample(w, rows, seed_offset=0, nthreads=None):
     return dt, flops, nt
 
 
+def oracle_decode_sample(w, heads, target_s, nthreads=None):
+    """Time the oracle's forward over `heads` heads of the decode workload
+    (nq query rows against all N cached keys each), repeated until about
+    target_s seconds have passed.  Returns (seconds, flops, threads, calls)."""
+    import torch
+    import oracle
+    nt = nthreads or oracle.default_threads()
+    g = torch.Generator()
+    g.manual_seed(int(w.seed) + 77)
+    k, v = (torch.randn((heads, w.N, w.d), generator=g).to(torch.bfloat16) for _ in range(2))
+    q = torch.randn((heads, w.nq, w.d), generator=g).to(torch.bfloat16)
+    qn, kn, vn = (oracle._f64(x) for x in (q, k, v))
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.fwd(qn, kn, vn, False, w.scale, nthreads=nt)
+        calls += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s:
+            break
+    return dt, calls * 4.0 * heads * w.nq * w.N * w.d, nt, calls
+
+
 def cpu_baseline(w, target_s=12.0):
+    if w.layout == "decode":
+        heads = min(w.B * w.H, 16)
+        dt, fl, nt, calls = oracle_decode_sample(w, heads, target_s)
+        return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                "sample": f"forward of {heads} of the {w.B * w.H} heads ({w.nq} query row(s) against all {w.N} "
+                          f"cached keys, d={w.d}), repeated {calls} times, fp64 C oracle, {dt:.1f} s"}
     # calibrate on a small sample, then size the timed one to ~target_s
     dt, fl, nt = oracle_sample(w, 64)
     rate = fl / max(dt, 1e-6)
@@ -183,6 +213,8 @@ def run_reference(args):
     if rank != 0:
         return
     w = workload(args)
+    if w.layout == "decode":
+        return run_reference_decode(args, w)
     # size each step so that warmup + steps take about 100 s in all
     dt, fl, nt = oracle_sample(w, 64)
     rate = fl / max(dt, 1e-6)
@@ -198,6 +230,28 @@ def run_reference(args):
     value = fl_total / t_total / 1e12
     sample = (f"per step: fwd+bwd of {rows} query rows of one head against all {w.N} keys, d={w.d}, "
               f"non-causal, fp64 C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_decode(args, w):
+    per_step_s = max(0.5, min(10.0, 100.0 / max(1, args.steps + args.warmup)))
+    heads = min(w.B * w.H, 16)
+    for _ in range(args.warmup):
+        oracle_decode_sample(w, heads, per_step_s)
+    t_total, fl_total, nt = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        dt, fl, nt, _ = oracle_decode_sample(w, heads, per_step_s)
+        t_total += dt
+        fl_total += fl
+    value = fl_total / t_total / 1e12
+    sample = (f"per step: forward of {heads} heads ({w.nq} query row(s) against all {w.N} cached keys, d={w.d}), "
+              f"repeated for about {per_step_s:.1f} s, fp64 C oracle")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -235,6 +289,8 @@ def token_rows(w):
 
 
 def touched_bytes(w):
+    if w.layout == "decode":  # the cache (k, v) plus q, o and lse
+        return 2 * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.nq * (2 * w.d * 2 + 4)
     n_t = 8 if w.backward else 4  # q, k, v, o (+ dO, dQ, dK, dV)
     return n_t * token_rows(w) * w.H * w.d * 2 + token_rows(w) * w.H * 4
 
@@ -254,6 +310,8 @@ def config_of(w):
         shape += " stored [B, N, H, d]"
     elif w.layout == "varlen":
         shape = f"T{token_rows(w)} ({w.B} packed sequences, longest {w.N}) H{w.H} d{w.d}"
+    elif w.layout == "decode":
+        shape = f"B{w.B} H{w.H} Nq{w.nq} against a cache of Nk{w.N} d{w.d}"
     c = {"workload": f"{'fwd+bwd' if w.backward else 'fwd'} {shape} "
                      f"{'causal' if w.causal else 'non-causal'} bf16",
          "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
@@ -262,6 +320,8 @@ def config_of(w):
          "l2": l2}
     if w.layout == "varlen":
         c["lengths"] = list(w.lengths)
+    if w.layout == "decode":
+        c["Nq"] = w.nq
     return c
 
 
@@ -278,6 +338,20 @@ class Problem:
         import exact_attention_48_gb300 as fa
         from exact_attention_48_gb300.inputs import draw, draw_shape
         self.w = w
+        if w.layout == "decode":
+            g = torch.Generator(device=device)
+            g.manual_seed(int(w.seed))
+            k, v = (torch.randn((w.B, w.H, w.N, w.d), generator=g, device=device).to(torch.bfloat16)
+                    for _ in range(2))
+            q = torch.randn((w.B, w.H, w.nq, w.d), generator=g, device=device).to(torch.bfloat16)
+            self.inputs = [q, k, v, None]
+            self.outputs = [torch.empty_like(q), None, None, None]
+            self.lse_shape = (w.B, w.H, w.nq)
+            self.lse = torch.empty(self.lse_shape, device=device, dtype=torch.float32)
+            self.ws = torch.empty(max(1, fa.fa_decode_workspace_bytes(w.B, w.H, w.nq, w.N, w.d)), device=device,
+                                  dtype=torch.uint8)
+            self._fa = fa
+            return
         if w.layout == "varlen":
             T = token_rows(w)
             q, k, v, do = draw_shape(1, w.H, T, w.d, w.seed, w.input_mult, device)
@@ -304,7 +378,9 @@ class Problem:
 
     def fwd(self, q, k, v, o, lse):
         w, fa, V = self.w, self._fa, self.view
-        if w.layout == "varlen":
+        if w.layout == "decode":
+            fa.fa_fwd_decode(q, k, v, None, w.causal, w.scale, o=o, lse=lse, workspace=self.ws)
+        elif w.layout == "varlen":
             fa.fa_fwd_varlen(q, k, v, self.cu, w.N, w.causal, w.scale, o=o, lse=lse)
         elif w.layout == "bnhd":
             fa.fa_fwd_strided(V(q), V(k), V(v), w.causal, w.scale, o=V(o), lse=lse)
@@ -461,6 +537,24 @@ def run_ours(args):
         "gpu_launches": (4 if bwd_on else 1) * args.steps,  # fwd; bwd pre, dK/dV, dQ
         "clocks": clk,
     }
+    if w.layout == "decode":
+        # HBM-bound: the roofline is bytes moved (the cache once, q, o, lse)
+        # over the call's time (the split kernel and, when the keys are cut
+        # into several chunks, the small merge kernel), against the measured
+        # copy bandwidth.
+        from exact_attention_48_gb300 import fa_decode_workspace_bytes
+        nbytes = touched_bytes(w)
+        gbs = nbytes / (fwd_ms * 1e-3) / 1e9
+        merged = fa_decode_workspace_bytes(w.B, w.H, w.nq, w.N, w.d) > 0
+        line["fwd"] = {"ms": fwd_ms, "tflops": fwd_tf, "gbs": gbs}
+        line["kernels"] = {"fa_decode_kernel" + (" + fa_decode_combine_kernel" if merged else ""):
+                           {"ms": fwd_ms, "gbs": gbs}}
+        line["roofline"] = {"bound": "hbm", "kernel": "fa_decode_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                            "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
+                            "bytes_per_launch": nbytes, "timed": "the whole call (split kernel + merge kernel)",
+                            "traffic": traffic_record("fa_decode_kernel", config_of(w)["workload"])}
+        line["gpu_launches"] = (2 if merged else 1) * args.steps
 
     if not args.no_e2e:
         line["e2e"] = e2e_leg(pb, args, world)
@@ -480,11 +574,11 @@ def e2e_leg(pb, args, world):
     import torch
     w = pb.w
     q = pb.inputs[0]
-    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in pb.inputs)
+    hq, hk, hv, hdo = (None if t is None else t.cpu().pin_memory() for t in pb.inputs)
     outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4)]
     hlse = torch.empty(pb.lse_shape, dtype=torch.float32).pin_memory()
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    q_, k_, v_, do_ = (torch.empty_like(q) for _ in range(4))
+    q_, k_, v_, do_ = (None if t is None else torch.empty_like(t) for t in pb.inputs)
     o_ = torch.empty_like(q)
     lse_ = torch.empty(pb.lse_shape, device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
@@ -513,8 +607,9 @@ def e2e_leg(pb, args, world):
     flops = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
     value, ms = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
     nbytes = q.numel() * q.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)[:n_in])
     return {"value": value, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": n_in * nbytes, "d2h_bytes_per_step": n_out * nbytes + hlse.numel() * 4,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n_out * nbytes + hlse.numel() * 4,
             "steps": steps}
 
 

@@ -10,8 +10,10 @@ from .binding import (  # noqa: F401
     fa_bwd_strided,
     fa_bwd_varlen,
     fa_bwd_workspace_bytes,
+    fa_decode_workspace_bytes,
     fa_device_status,
     fa_fwd,
+    fa_fwd_decode,
     fa_fwd_strided,
     fa_fwd_varlen,
     library,

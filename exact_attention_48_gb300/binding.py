@@ -74,6 +74,11 @@ def library(path: str | None = None):
             lib.fa_bwd_varlen.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, p64, vp, p64,
                                           vp, p64, vp, i, i, i, i, i, i, f, vp, sz, vp]
             lib.fa_bwd_varlen.restype = i
+            lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+            lib.fa_decode_workspace_bytes.restype = sz
+            lib.fa_fwd_decode.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, i, i, i, i, i, i, f, vp, sz,
+                                          vp]
+            lib.fa_fwd_decode.restype = i
             lib.fa_status_string.argtypes = [i]
             lib.fa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -256,6 +261,54 @@ def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bo
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(library().fa_decode_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_fwd_decode(q, k, v, cache_seqlens=None, causal: bool = False, scale: float | None = None, o=None, lse=None,
+                  workspace=None, stream=None):
+    """Decode forward: q [B, H, Nq, d] (Nq <= 8, the last Nq positions)
+    against a key/value cache k, v [B, H, Nk, d] (views with contiguous d,
+    e.g. ``cache.transpose(1, 2)`` of a [B, Nk, H, d] cache), of which the
+    first cache_seqlens[b] rows are valid (int32 CUDA tensor [B], or None
+    for all Nk).  Returns (o [B, H, Nq, d] bf16, lse [B, H, Nq] fp32)."""
+    _check_view("q", q)
+    B, H, Nq, d = q.shape
+    _check_view("k", k)
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d):
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected ({B}, {H}, Nk, {d})")
+    _check_view("v", v, k.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty(q.shape, device=q.device, dtype=q.dtype)
+    else:
+        _check_view("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    cl = None
+    if cache_seqlens is not None:
+        if not isinstance(cache_seqlens, torch.Tensor) or not cache_seqlens.is_cuda \
+                or cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,) \
+                or not cache_seqlens.is_contiguous():
+            raise ValueError("cache_seqlens must be a contiguous int32 CUDA tensor [B]")
+        cl = cache_seqlens.data_ptr()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = library().fa_fwd_decode(q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v),
+                                 o.data_ptr(), _strides(o), lse.data_ptr(), cl, B, H, Nq, Nk, d, int(bool(causal)),
+                                 float(scale), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_decode")
+    return o, lse
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):

@@ -343,6 +343,168 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   return rc;
 }
 
+// ------------------------------------------------------------------ decode
+
+constexpr int kDecodeMaxNq = 8;
+constexpr int kDecodeModelCtas = 152;  // GB300's SMs: the persistent grid the split plan is made for
+constexpr int kDecodeMaxSplits = 64;
+
+struct DecodePlan {
+  int chunk, splits;
+};
+
+// Chunk size (in 128-key tiles) for the persistent decode grid: the one
+// whose round-robin assignment of (chunk, head) items to kDecodeModelCtas
+// CTAs gives the smallest busiest-CTA load, counting each item's fixed
+// merge cost as a quarter tile; ties go to larger chunks (fewer partials).
+// A function of the shape alone, so the workspace size is too.
+DecodePlan plan_decode(long long BH, int tiles) {
+  thread_local long long last_bh = -1;
+  thread_local int last_tiles = -1;
+  thread_local DecodePlan last{1, 1};
+  if (BH == last_bh && tiles == last_tiles) return last;
+  const double alpha = 0.25;
+  DecodePlan best{tiles, 1};
+  double best_cost = 1e300;
+  int prev = -1;
+  for (int sp = 1; sp <= tiles && sp <= kDecodeMaxSplits; ++sp) {
+    const int chunk = (tiles + sp - 1) / sp;
+    if (chunk == prev) continue;
+    prev = chunk;
+    const int splits = (tiles + chunk - 1) / chunk;
+    const int tail = tiles - (splits - 1) * chunk;
+    const long long F = (splits - 1) * BH, I = splits * BH;
+    const long long G = I < kDecodeModelCtas ? I : kDecodeModelCtas;
+    double cost = 0.0;
+    for (long long j = 0; j < G; ++j) {
+      const long long nf = F / G + (j < F % G ? 1 : 0);
+      const long long ni = I / G + (j < I % G ? 1 : 0);
+      const double load = nf * (chunk + alpha) + (ni - nf) * (tail + alpha);
+      cost = load > cost ? load : cost;
+    }
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = DecodePlan{chunk, splits};
+    }
+  }
+  last_bh = BH;
+  last_tiles = tiles;
+  last = best;
+  return best;
+}
+
+fa_status_t check_decode(int B, int H, int Nq, int Nk, int d, int causal, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARGUMENT;
+  if (Nq > kDecodeMaxNq) return FA_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
+  if (d != 64 && d != 128) return d < 1 ? FA_ERR_INVALID_ARGUMENT : FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H >= (1LL << 24)) return FA_ERR_INVALID_ARGUMENT;
+  if (Nk > (1 << 30)) return FA_ERR_INVALID_ARGUMENT;
+  return FA_OK;
+}
+
+size_t decode_workspace(int B, int H, int Nq, int Nk, int d) {
+  const long long BH = static_cast<long long>(B) * H;
+  const DecodePlan pl = plan_decode(BH, (Nk + 127) / 128);
+  if (pl.splits == 1) return 0;
+  const size_t parts = static_cast<size_t>(BH) * pl.splits * Nq;
+  return round256(parts * d * 4) + round256(parts * 4);
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  thread_local int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+fa_status_t decode_impl(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                        const void *v, const int64_t *v_strides, void *o, const int64_t *o_strides, float *lse,
+                        const int *cache_len, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  fa_status_t st = check_decode(B, H, Nq, Nk, d, causal, scale);
+  if (st != FA_OK) return st;
+  const void *ptrs[5] = {q, k, v, o, lse};
+  for (const void *x : ptrs)
+    if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+  if (cache_len && (reinterpret_cast<uintptr_t>(cache_len) & 3u)) return FA_ERR_INVALID_ARGUMENT;
+  Strides sq, sk, sv, so;
+  if (!normalise(q_strides, B, H, Nq, d, &sq) || !normalise(k_strides, B, H, Nk, d, &sk) ||
+      !normalise(v_strides, B, H, Nk, d, &sv) || !normalise(o_strides, B, H, Nq, d, &so))
+    return FA_ERR_INVALID_ARGUMENT;
+  if (!injective(B, H, Nq, d, so)) return FA_ERR_INVALID_ARGUMENT;
+  // no output may share memory with an input, the other output or the workspace
+  uintptr_t lo[6], hi[6];  // q, k, v, cache_len, o, lse
+  span(q, B, H, Nq, d, sq, &lo[0], &hi[0]);
+  span(k, B, H, Nk, d, sk, &lo[1], &hi[1]);
+  span(v, B, H, Nk, d, sv, &lo[2], &hi[2]);
+  lo[3] = reinterpret_cast<uintptr_t>(cache_len);
+  hi[3] = cache_len ? lo[3] + static_cast<size_t>(B) * 4 : lo[3];
+  span(o, B, H, Nq, d, so, &lo[4], &hi[4]);
+  lo[5] = reinterpret_cast<uintptr_t>(lse);
+  hi[5] = lo[5] + static_cast<size_t>(B) * H * Nq * 4;
+  for (int out = 4; out < 6; ++out)
+    for (int i = 0; i < 6; ++i) {
+      if (i == out || (out == 5 && i == 4)) continue;
+      if (out == 4 && i == 0) {
+        if (may_overlap(q, sq, o, so, B, H, Nq, d)) return FA_ERR_INVALID_ARGUMENT;
+      } else if (spans_overlap(lo[i], hi[i], lo[out], hi[out])) {
+        return FA_ERR_INVALID_ARGUMENT;
+      }
+    }
+  const long long BH = static_cast<long long>(B) * H;
+  const int tiles = (Nk + 127) / 128;
+  const DecodePlan pl = plan_decode(BH, tiles);
+  const size_t need = decode_workspace(B, H, Nq, Nk, d);
+  if (workspace && need) {
+    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID_ARGUMENT;
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+    for (int i = 0; i < 6; ++i)
+      if (spans_overlap(lo[i], hi[i], wlo, whi)) return FA_ERR_INVALID_ARGUMENT;
+  }
+
+  CUtensorMap tk, tv;
+  if (!encode_map(&tk, k, B, H, Nk, d, sk) || !encode_map(&tv, v, B, H, Nk, d, sv)) return FA_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return FA_ERR_CUDA;
+  void *ws = need ? workspace : nullptr;
+  bool owned = false;
+  if (need && !ws) {
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return FA_ERR_CUDA;
+    owned = true;
+  }
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.sq = sq;
+  p.so = so;
+  p.cache_len = cache_len;
+  const size_t parts = static_cast<size_t>(BH) * pl.splits * Nq;
+  p.part_o = need ? static_cast<float *>(ws) : nullptr;
+  p.part_lse = need ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round256(parts * d * 4)) : nullptr;
+  p.status = status_ptr();
+  p.H = H;
+  p.BH = static_cast<int>(BH);
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.chunk = pl.chunk;
+  p.splits = pl.splits;
+  p.items = static_cast<int>(BH * pl.splits);
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = p.items < sms ? p.items : sms;
+  fa_status_t rc = FA_OK;
+  if (!p.status || launch_decode(d, tk, tv, p, grid, stream) != cudaSuccess) rc = FA_ERR_CUDA;
+  if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
+  return rc;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -438,6 +600,19 @@ fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const void *k
     if (!normalise_packed(in[i], H, T, d, &s[i])) return FA_ERR_INVALID_ARGUMENT;
   return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7],
                   RowAxis{B, max_seqlen, cu_seqlens, T}, H, d, causal, scale, workspace, workspace_bytes, stream);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode(B, H, Nq, Nk, d, 0, 1.0f) != FA_OK) return 0;
+  return decode_workspace(B, H, Nq, Nk, d);
+}
+
+fa_status_t fa_fwd_decode(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,
+                          const void *v, const int64_t *v_strides, void *o, const int64_t *o_strides, float *lse,
+                          const int *cache_seqlens, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_impl(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, cache_seqlens, B, H, Nq, Nk, d,
+                     causal, scale, workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_device_status(cudaStream_t stream) {

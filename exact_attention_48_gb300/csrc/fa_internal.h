@@ -26,6 +26,7 @@ enum WaitSite : int {
   kSiteDqEmpty,
   kSiteKvFull,
   kSiteMmaDone,
+  kSiteKvEmpty,
 };
 
 // Element strides of a [B, H, N, d] bf16 tensor whose d elements are
@@ -95,6 +96,29 @@ struct BwdParams {
   float scale;
   float scale_log2;
 };
+
+// Decode forward: Nq (<= 8) query rows per head against Nk cached keys.
+// The keys of a head are cut into chunks of `chunk` 128-key tiles; item
+// it = split * BH + bh is chunk `split` of head bh.  With splits > 1 each
+// item writes its normalised partial O and log2-domain logsumexp to
+// part_o / part_lse and a second kernel merges them.
+struct DecodeParams {
+  const __nv_bfloat16 *q;     // [B, H, Nq, d] strides sq
+  __nv_bfloat16 *o;           // [B, H, Nq, d] strides so
+  float *lse;                 // [B, H, Nq] contiguous (natural log)
+  Strides sq, so;
+  const int *cache_len;       // [B] valid keys per batch entry (device), or null: all Nk
+  float *part_o;              // [BH][splits][Nq][d] fp32 (splits > 1)
+  float *part_lse;            // [BH][splits][Nq] fp32, log2 units (splits > 1)
+  int *status;
+  int H, BH, Nq, Nk;
+  int chunk, splits, items;
+  int causal;                 // query i sees keys j <= len - Nq + i
+  float scale_log2;           // scale * log2(e)
+};
+
+cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
+                          cudaStream_t stream);
 
 // Tensor maps over [B, H, N, d] bf16 tensors viewed as 4-D (d, N, H, B)
 // with the tensors' strides, box (64, 128, 1, 1), 128-byte swizzle.

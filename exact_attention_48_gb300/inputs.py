@@ -29,8 +29,10 @@ class Workload:
     input_mult: float = 1.0   # Q/K/V are N(0,1) * input_mult (dO stays N(0,1))
     seed: int = 1000
     note: str = field(default="", compare=False)
-    layout: str = "bhnd"      # "bhnd" contiguous, "bnhd" ([B, N, H, d] storage), "varlen" (packed sequences)
+    layout: str = "bhnd"      # "bhnd" contiguous, "bnhd" ([B, N, H, d] storage), "varlen" (packed sequences),
+                              # "decode" (nq query rows against a cache of N keys)
     lengths: tuple = ()       # varlen: the B sequence lengths (N is the longest)
+    nq: int = 0               # decode: query rows per head
 
     @property
     def scale(self) -> float:
@@ -39,6 +41,8 @@ class Workload:
     def flops_fwd(self) -> float:
         if self.layout == "varlen":
             f = sum(4.0 * self.H * n * n * self.d for n in self.lengths)
+        elif self.layout == "decode":
+            f = 4.0 * self.B * self.H * self.nq * self.N * self.d
         else:
             f = 4.0 * self.B * self.H * self.N * self.N * self.d
         return f / 2 if self.causal else f
@@ -88,6 +92,11 @@ BNHD_B2H16N8192D128 = Workload("bnhd_b2h16n8192d128", 2, 16, 8192, 128, False, T
 _VL = varlen_lengths(16384, 256, 4096, 1006)
 VARLEN_T16384H16D128 = Workload("varlen_t16384h16d128_causal", len(_VL), 16, max(_VL), 128, True, True, 1.0,
                                 1006, "packed sequences of 256..4096 tokens", layout="varlen", lengths=_VL)
+
+# Decoding one token per sequence against a 16384-token key/value cache
+# (bf16, contiguous [B, H, N, d] cache): HBM-bound, 2 GiB of cache per step.
+DECODE_B16H16NK16384D128 = Workload("decode_b16h16nk16384d128", 16, 16, 16384, 128, False, False, 1.0, 1007,
+                                    "one query row per head against a 16384-key cache", layout="decode", nq=1)
 
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
 HEADLINE = sweep(8192, 128, False)   # B=2, H=16, N=8192, d=128, non-causal

@@ -178,6 +178,51 @@ FA_API fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const 
                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Decode forward: Nq new query rows per (batch entry, head) against a cache
+ * of keys and values, as in token-by-token generation.  The computation is
+ * the forward pass above (o and lse, same definition and scale), with
+ * rectangular shapes: per (b, h) the query rows are q[b, h, 0..Nq) and the
+ * keys/values are the first len_b rows of the cache, len_b = cache_seqlens[b]
+ * (all Nk rows when cache_seqlens is NULL).  The query rows are the LAST Nq
+ * positions of the sequence: with causal = 1, query i sees key j iff
+ * j <= len_b - Nq + i (mask aligned at the bottom-right; for Nq = 1 it is no
+ * restriction); with causal = 0 it sees every key j < len_b.  A query row
+ * that sees no key (len_b = 0, or causal with len_b - Nq + i < 0) gets
+ * o = 0 and lse = -inf.
+ *   q    : [B, H, Nq, d] bf16, element strides q_strides[3] (b, h, row)
+ *   k, v : [B, H, Nk, d] bf16, element strides k_strides / v_strides (a
+ *          cache stored [B, Nk, H, d] is strides {Nk*H*d, d, H*d})
+ *   o    : [B, H, Nq, d] bf16, strides o_strides; must not overlap anything
+ *   lse  : [B, H, Nq] fp32, contiguous
+ *   cache_seqlens : NULL, or a device array of B int32 (4-byte aligned);
+ *          the kernel clamps each value into [0, Nk], so a bad value gives a
+ *          wrong result for its batch entry, never an access outside k, v
+ *   1 <= Nq <= 8, Nk >= 1 (Nk <= 2^30), d 64 or 128, B*H < 2^24; strides
+ *   follow the rules of the *_strided calls.
+ *   workspace : device scratch of fa_decode_workspace_bytes(B, H, Nq, Nk, d)
+ *          bytes (256-byte aligned; that size may be 0), or NULL to let the
+ *          call take it with cudaMallocAsync/cudaFreeAsync on `stream`.
+ * Work is split over the keys: each 128-key tile chunk of a head gives a
+ * partial result normalised over its own keys and its logsumexp, and the
+ * partials are merged with the same running-maximum correction the tiled
+ * pass uses between key blocks; the chunk size depends on the shape only,
+ * so the result is bitwise reproducible for the same inputs.  The
+ * glossary page "FlashAttention" (blog.brdg.mn) places the method in model
+ * serving next to the block-wise management of the key/value cache
+ * (sections "Der Engpass ist der Weg zum Speicher, nicht das Rechnen" and
+ * "Wo es verwechselt wird"); decoding against that cache is this call.
+ * The cache's block management itself is not part of the library.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+FA_API fa_status_t fa_fwd_decode(const void *q, const int64_t *q_strides, const void *k,
+                                 const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                                 void *o, const int64_t *o_strides, float *lse,
+                                 const int *cache_seqlens, int B, int H, int Nq, int Nk, int d,
+                                 int causal, float scale, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * Size in bytes of the fixed device array that fa_bwd_noalloc uses as its
  * scratch (8 MiB).  Every GPU that loads the library holds this array until
  * the process exits.  It covers B * H * Np <= 1,048,576 padded rows, where

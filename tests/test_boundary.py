@@ -169,3 +169,48 @@ def test_varlen_rejects(lib):
     assert fwd(o=FAKE + (2 << 30) + 1024) == FA_ERR_INVALID_ARGUMENT                     # o inside v
     assert lib.fa_bwd_varlen(FAKE, c, FAKE, c, FAKE, c, FAKE, c, FAKE, c, FAKE, FAKE, c, FAKE, c, FAKE, c, None,
                              3, H, T, 200, d, 0, 0.125, None, 0, None) == FA_ERR_INVALID_ARGUMENT
+
+
+def test_decode_workspace_bytes(lib):
+    # one 128-key tile per head: a single chunk, nothing to merge
+    assert lib.fa_decode_workspace_bytes(8, 32, 1, 128, 64) == 0
+    # a long cache over few heads: several chunks, partial O (fp32) + lse per chunk
+    need = lib.fa_decode_workspace_bytes(1, 2, 2, 40000, 128)
+    assert need > 0 and need % 256 == 0
+    assert lib.fa_decode_workspace_bytes(0, 1, 1, 128, 64) == 0       # invalid shape
+    assert lib.fa_decode_workspace_bytes(1, 1, 9, 4096, 64) == 0      # Nq above 8
+    assert lib.fa_decode_workspace_bytes(1, 1, 1, 4096, 96) == 0      # unsupported d
+
+
+def test_decode_rejects(lib):
+    B, H, Nq, Nk, d = 2, 2, 2, 1000, 64
+    cq = _s(H * Nq * d, Nq * d, d)
+    ck = _s(H * Nk * d, Nk * d, d)
+    need = lib.fa_decode_workspace_bytes(B, H, Nq, Nk, d)
+
+    def call(q=FAKE, qs=cq, k=FAKE + (1 << 30), ks=ck, v=FAKE + (2 << 30), o=FAKE + (3 << 30), os_=cq,
+             lse=FAKE + (4 << 30), cl=None, b=B, nq=Nq, nk=Nk, dd=d, causal=0, scale=0.125, ws=None, ws_bytes=0):
+        return lib.fa_fwd_decode(q, qs, k, ks, v, ks, o, os_, lse, cl, b, H, nq, nk, dd, causal, scale, ws,
+                                 ws_bytes, None)
+    assert call(nq=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(nq=9) == FA_ERR_INVALID_ARGUMENT
+    assert call(nk=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(b=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(dd=96) == FA_ERR_UNSUPPORTED
+    assert call(causal=2) == FA_ERR_INVALID_ARGUMENT
+    assert call(scale=float("nan")) == FA_ERR_INVALID_ARGUMENT
+    assert call(q=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(lse=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(cl=FAKE + (6 << 30) + 2) == FA_ERR_INVALID_ARGUMENT                   # misaligned lengths
+    assert call(qs=None) == FA_ERR_INVALID_ARGUMENT
+    assert call(ks=_s(H * Nk * d, Nk * d, d + 4)) == FA_ERR_INVALID_ARGUMENT           # row stride not x8
+    assert call(os_=_s(H * Nq * d, Nq * d, 8)) == FA_ERR_INVALID_ARGUMENT              # rows of o overlap
+    assert call(o=FAKE + 64) == FA_ERR_INVALID_ARGUMENT                               # o overlaps q
+    assert call(o=FAKE + (1 << 30) + 4096) == FA_ERR_INVALID_ARGUMENT                 # o inside the key cache
+    assert call(lse=FAKE + (2 << 30) + 256) == FA_ERR_INVALID_ARGUMENT                # lse inside the value cache
+    assert call(lse=FAKE + (3 << 30) + 16) == FA_ERR_INVALID_ARGUMENT                 # lse overlaps o
+    assert call(cl=FAKE + (3 << 30)) == FA_ERR_INVALID_ARGUMENT                       # lengths inside o
+    if need:
+        assert call(ws=FAKE + (20 << 30), ws_bytes=need - 1) == FA_ERR_WORKSPACE
+        assert call(ws=FAKE + (20 << 30) + 16, ws_bytes=need) == FA_ERR_INVALID_ARGUMENT
+        assert call(ws=FAKE + (1 << 30), ws_bytes=need) == FA_ERR_INVALID_ARGUMENT    # workspace inside k
