@@ -52,6 +52,13 @@ def _bind(path: str):
     lib.oracle_probs.restype = I
     lib.oracle_fwd_spread.argtypes = [dp, dp, dp, dp, L, L, L, L, I, D, I]
     lib.oracle_fwd_spread.restype = I
+    u8 = ctypes.POINTER(ctypes.c_uint8)
+    lib.e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.e4m3_value.restype = D
+    lib.e4m3_round.argtypes = [D]
+    lib.e4m3_round.restype = D
+    lib.oracle_fwd_fp8.argtypes = [u8, u8, u8, D, D, D, dp, dp, dp, L, L, L, L, I, D, D, I]
+    lib.oracle_fwd_fp8.restype = I
     return lib
 
 
@@ -156,3 +163,48 @@ def fwd_spread(q, k, v, causal: bool, scale: float, nthreads: int | None = None,
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_spread failed ({rc})")
     return out
+
+
+# ---------------------------------------------------------------- FP8
+
+def e4m3_value(code: int, lib=None) -> float:
+    """Value of one e4m3 code (the format's definition, written out in C)."""
+    return float((lib or _load()).e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_round(x: float, lib=None) -> float:
+    """Nearest e4m3 value (ties to even, saturated to +-448)."""
+    return float((lib or _load()).e4m3_round(float(x)))
+
+
+def _u8(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor (float8_e4m3fn or uint8): its bytes
+        import torch
+        t = x.detach().to("cpu").contiguous()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        x = t.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+
+
+def fwd_fp8(q8, k8, v8, sq: float, sk: float, sv: float, causal: bool, scale: float, acc_rel: float = 0.0,
+            with_bound: bool = False, nthreads: int | None = None, lib=None):
+    """FP8 forward (the definition in attn_oracle.c): e4m3 codes [..., N, d]
+    (uint8 arrays or float8_e4m3fn tensors) and tensor scales.  Returns
+    (o, lse) in fp64, and the per-element bound when with_bound."""
+    q, k, v = _u8(q8), _u8(k8), _u8(v8)
+    lead, BH, Nq, Nk, d = _shape(q, k)
+    if v.shape != k.shape:
+        raise ValueError("v must have the shape of k")
+    o = np.empty(q.shape, np.float64)
+    lse = np.empty(lead + (Nq,), np.float64)
+    bound = np.empty(q.shape, np.float64) if with_bound else None
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    rc = (lib or _load()).oracle_fwd_fp8(q.ctypes.data_as(u8p), k.ctypes.data_as(u8p), v.ctypes.data_as(u8p),
+                                         float(sq), float(sk), float(sv), _ptr(o), _ptr(lse),
+                                         _ptr(bound) if with_bound else None, BH, Nq, Nk, d,
+                                         int(bool(causal)), float(scale), float(acc_rel),
+                                         nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_fwd_fp8 failed ({rc})")
+    return (o, lse, bound) if with_bound else (o, lse)

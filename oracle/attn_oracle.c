@@ -364,3 +364,219 @@ int oracle_probs(const double *q, const double *k, double *p, long Nq, long Nk,
     pthread_mutex_destroy(&J.mu);
     return 0;
 }
+
+/* ------------------------------------------------------------------ FP8
+ *
+ * The FP8 forward.  The page "FlashAttention-2 (DE)", section
+ * "Vergleich mit nachfolgenden Versionen" / "FlashAttention-3", names FP8
+ * (low precision) as one of FlashAttention-3's additions and gives no
+ * formula.  The reading implemented here (and by the GPU path):
+ *
+ *  - Q, K, V arrive as e4m3 codes q8, k8, v8 with one scale per tensor:
+ *    the value of code c of tensor X is e4m3_value(c) * sX.
+ *  - Scores are exact on those values: x_ij = s * log2(e) * sum_c q_ic k_jc
+ *    (log2 units), x_ij = -inf for keys the mask hides.
+ *  - M_i = ceil(max_j x_ij), an integer.  The weight that multiplies v_j is
+ *    the probability rounded to e4m3 at that power-of-two scale:
+ *    w_ij = e4m3_round(2^(x_ij - M_i + 8)), a value in [0, 256].
+ *  - O_i = sv * sum_j w_ij v_j / sum_j w_ij (the rounded weights are what
+ *    is applied, and they are normalised by their own sum);
+ *    LSE_i = ln(2) * (M_i - 8 + log2 sum_j 2^(x_ij - M_i + 8)), the exact
+ *    logsumexp of the scaled scores.
+ *
+ * Because M_i is an integer and e4m3 rounding commutes with multiplication
+ * by a power of two while the value stays in the normal range, the weights
+ * do not depend on how a tiled implementation walks the keys (the running
+ * maximum it uses is an integer too).  Only weights below the normal range
+ * (2^(x - M + 8) < 2^-6) do; oracle_fwd_fp8 reports a per-element bound
+ * for them and for weights whose rounding the GPU's fp32 scores could tip.
+ *
+ * The e4m3 format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 holds the subnormals m * 2^-9; exponent 15 with mantissa
+ * 7 is NaN; there are no infinities; the largest finite value is 448.
+ */
+
+double e4m3_value(unsigned char code)
+{
+    int sgn = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Nearest e4m3 value to x, ties to the even mantissa, magnitudes above 448
+ * saturated to 448 (the GPU converts with saturation to the finite range). */
+double e4m3_round(double x)
+{
+    if (isnan(x)) return NAN;
+    double a = fabs(x);
+    if (a == 0.0) return x;
+    int ex;
+    frexp(a, &ex);                     /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                    /* binade: 2^e <= a < 2^(e+1) */
+    if (e < -6) e = -6;                /* subnormal spacing below 2^-6 */
+    double ulp = ldexp(1.0, e - 3);
+    double r = nearbyint(a / ulp) * ulp;   /* default rounding: ties to even */
+    if (r > 448.0) r = 448.0;
+    return x < 0 ? -r : r;
+}
+
+typedef struct {
+    const unsigned char *q8, *k8, *v8;
+    double sq, sk, sv;
+    double *o, *lse, *bound;
+    long BH, Nq, Nk, d;
+    int causal;
+    double scale;
+    double acc_rel;     /* relative precision assumed for the GPU's fp32 score sums */
+    long rows_per_item, items_per_head, next_item;
+    pthread_mutex_t mu;
+} fp8_job_t;
+
+static int fp8_take(fp8_job_t *J, long *item)
+{
+    pthread_mutex_lock(&J->mu);
+    long it = J->next_item++;
+    pthread_mutex_unlock(&J->mu);
+    if (it >= J->BH * J->items_per_head) return 0;
+    *item = it;
+    return 1;
+}
+
+static void *fp8_worker(void *arg)
+{
+    fp8_job_t *J = (fp8_job_t *)arg;
+    const long d = J->d;
+    const double c = J->scale * J->sq * J->sk / log(2.0);   /* s * log2(e) * sq * sk */
+    double *x = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *w = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *dw = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)J->Nk * d);
+    if (!x || !w || !dw || !qd || !vd) { free(x); free(w); free(dw); free(qd); free(vd); return (void *)1; }
+    long item;
+    long vh_loaded = -1;
+    while (fp8_take(J, &item)) {
+        long h = item / J->items_per_head;
+        long r0 = (item % J->items_per_head) * J->rows_per_item;
+        long r1 = r0 + J->rows_per_item;
+        if (r1 > J->Nq) r1 = J->Nq;
+        const unsigned char *kh = J->k8 + h * J->Nk * d;
+        if (vh_loaded != h) {
+            const unsigned char *vh = J->v8 + h * J->Nk * d;
+            for (long t = 0; t < J->Nk * d; ++t) vd[t] = e4m3_value(vh[t]);
+            vh_loaded = h;
+        }
+        for (long i = r0; i < r1; ++i) {
+            const unsigned char *qi = J->q8 + (h * J->Nq + i) * d;
+            for (long cc = 0; cc < d; ++cc) qd[cc] = e4m3_value(qi[cc]);
+            long end = J->causal ? (i + 1 < J->Nk ? i + 1 : J->Nk) : J->Nk;
+            double mx = -INFINITY;
+            for (long j = 0; j < end; ++j) {
+                const unsigned char *kj = kh + j * d;
+                double acc = 0.0, mag = 0.0;
+                for (long cc = 0; cc < d; ++cc) {
+                    double t = qd[cc] * e4m3_value(kj[cc]);
+                    acc += t;
+                    mag += fabs(t);
+                }
+                x[j] = c * acc;
+                dw[j] = fabs(c) * mag;      /* for the bound below */
+                if (x[j] > mx) mx = x[j];
+            }
+            double M = ceil(mx);
+            double W = 0.0, Z = 0.0;
+            for (long j = 0; j < end; ++j) {
+                double y = exp2(x[j] - M + 8.0);
+                w[j] = e4m3_round(y);
+                W += w[j];
+                Z += y;
+                /* Bound on |w_gpu - w_oracle|: the GPU computes y from fp32
+                 * scores (error <= acc_rel * |c| * sum|q k| + 2^-23 |x|) and
+                 * exp2 in fp32 (relative 2^-21): if y lies that close to a
+                 * rounding midpoint, its rounding may go the other way (one
+                 * ulp).  Below the normal range (one binade of margin for
+                 * the GPU's maximum), the GPU rounds on a grid that depends
+                 * on its running maximum: at most one subnormal step. */
+                double dx = J->acc_rel * dw[j] + ldexp(fabs(x[j]), -23);
+                double rel = 0.6931471805599453 * dx + ldexp(1.0, -21);
+                double delta = 0.0;
+                if (y < ldexp(1.0, -5)) {
+                    delta = ldexp(1.0, -9);
+                } else {
+                    int ex;
+                    frexp(y, &ex);
+                    double ulp = ldexp(1.0, ex - 1 - 3);
+                    double mid = (floor(y / ulp) + 0.5) * ulp;
+                    if (fabs(y - mid) <= rel * y) delta = ulp;
+                }
+                dw[j] = delta;
+            }
+            double *oi = J->o + (h * J->Nq + i) * d;
+            for (long cc = 0; cc < d; ++cc) {
+                double acc = 0.0;
+                for (long j = 0; j < end; ++j) acc += w[j] * vd[j * d + cc];
+                oi[cc] = J->sv * acc / W;
+            }
+            if (J->lse) J->lse[h * J->Nq + i] = log(2.0) * (M - 8.0 + log2(Z));
+            if (J->bound) {
+                double dsum = 0.0;
+                for (long j = 0; j < end; ++j) dsum += dw[j];
+                double *bi = J->bound + (h * J->Nq + i) * d;
+                for (long cc = 0; cc < d; ++cc) {
+                    double o_c = oi[cc] / J->sv, b = 0.0;
+                    for (long j = 0; j < end; ++j)
+                        if (dw[j] > 0.0) b += dw[j] * fabs(vd[j * d + cc] - o_c);
+                    bi[cc] = (W - dsum > 0.0) ? fabs(J->sv) * b / (W - dsum) : INFINITY;
+                }
+            }
+        }
+    }
+    free(x); free(w); free(dw); free(qd); free(vd);
+    return NULL;
+}
+
+/* FP8 forward of e4m3 codes q8[BH][Nq][d], k8/v8[BH][Nk][d] with tensor
+ * scales sq, sk, sv: o[BH][Nq][d], lse[BH][Nq] (may be NULL) as defined
+ * above, and optionally bound[BH][Nq][d]: how far a GPU result may lie from
+ * o because of the weights whose rounding the GPU may take differently
+ * (acc_rel = relative precision of the GPU's fp32 score sums). */
+int oracle_fwd_fp8(const unsigned char *q8, const unsigned char *k8, const unsigned char *v8,
+                   double sq, double sk, double sv, double *o, double *lse, double *bound,
+                   long BH, long Nq, long Nk, long d, int causal, double scale, double acc_rel,
+                   int nthreads)
+{
+    if (check_args(BH, Nq, Nk, d, causal) || !q8 || !k8 || !v8 || !o) return -1;
+    fp8_job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q8 = q8; J.k8 = k8; J.v8 = v8;
+    J.sq = sq; J.sk = sk; J.sv = sv;
+    J.o = o; J.lse = lse; J.bound = bound;
+    J.BH = BH; J.Nq = Nq; J.Nk = Nk; J.d = d;
+    J.causal = causal; J.scale = scale; J.acc_rel = acc_rel;
+    long want = (long)(nthreads > 0 ? nthreads : 1) * 4;
+    long per_head = (want + BH - 1) / BH;
+    if (per_head < 1) per_head = 1;
+    if (per_head > Nq) per_head = Nq;
+    J.rows_per_item = (Nq + per_head - 1) / per_head;
+    J.items_per_head = (Nq + J.rows_per_item - 1) / J.rows_per_item;
+    pthread_mutex_init(&J.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    int started = 0, failed = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, fp8_worker, &J) != 0) break;
+        ++started;
+    }
+    if (started == 0) failed = fp8_worker(&J) != NULL;
+    for (int t = 0; t < started; ++t) {
+        void *r = NULL;
+        pthread_join(th[t], &r);
+        if (r) failed = 1;
+    }
+    pthread_mutex_destroy(&J.mu);
+    return failed ? -2 : 0;
+}
