@@ -45,7 +45,8 @@ def parse_args():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--workload", choices=["sweep", "fwd_b8h16n2048d64", "causal_b4h32n4096d128",
                                            "long_b1h16n16384d128x2", "bnhd_b2h16n8192d128",
-                                           "varlen_t16384h16d128_causal", "decode_b16h16nk16384d128"],
+                                           "varlen_t16384h16d128_causal", "decode_b16h16nk16384d128",
+                                           "fp8_b2h16n8192d128"],
                     default="sweep",
                     help="a named workload instead of the sweep point given by --N/--d/--causal "
                          "(the forward-only one times the forward alone)")
@@ -62,7 +63,8 @@ def workload(args):
              "long_b1h16n16384d128x2": inputs.LONG_B1H16N16384D128,
              "bnhd_b2h16n8192d128": inputs.BNHD_B2H16N8192D128,
              "varlen_t16384h16d128_causal": inputs.VARLEN_T16384H16D128,
-             "decode_b16h16nk16384d128": inputs.DECODE_B16H16NK16384D128}
+             "decode_b16h16nk16384d128": inputs.DECODE_B16H16NK16384D128,
+             "fp8_b2h16n8192d128": inputs.FP8_B2H16N8192D128}
     if getattr(args, "workload", "sweep") != "sweep":
         return named[args.workload]
     return inputs.sweep(args.N, args.d, args.causal)
@@ -291,6 +293,8 @@ def token_rows(w):
 def touched_bytes(w):
     if w.layout == "decode":  # the cache (k, v) plus q, o and lse
         return 2 * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.nq * (2 * w.d * 2 + 4)
+    if w.layout == "fp8":  # q, k, v one byte per element, o bf16, lse
+        return w.B * w.H * w.N * (3 * w.d + 2 * w.d + 4)
     n_t = 8 if w.backward else 4  # q, k, v, o (+ dO, dQ, dK, dV)
     return n_t * token_rows(w) * w.H * w.d * 2 + token_rows(w) * w.H * 4
 
@@ -312,11 +316,14 @@ def config_of(w):
         shape = f"T{token_rows(w)} ({w.B} packed sequences, longest {w.N}) H{w.H} d{w.d}"
     elif w.layout == "decode":
         shape = f"B{w.B} H{w.H} Nq{w.nq} against a cache of Nk{w.N} d{w.d}"
+    elif w.layout == "fp8":
+        shape = f"B{w.B} H{w.H} N{w.N} d{w.d} e4m3 inputs"
     c = {"workload": f"{'fwd+bwd' if w.backward else 'fwd'} {shape} "
-                     f"{'causal' if w.causal else 'non-causal'} bf16",
+                     f"{'causal' if w.causal else 'non-causal'}{'' if w.layout == 'fp8' else ' bf16'}",
          "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
          "layout": w.layout,
-         "inputs": f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}",
+         "inputs": (f"i.i.d. N(0,1) x{w.input_mult:g}, per-tensor e4m3 (scale amax/448), seed {w.seed}"
+                    if w.layout == "fp8" else f"i.i.d. N(0,1) x{w.input_mult:g} bf16, seed {w.seed}"),
          "l2": l2}
     if w.layout == "varlen":
         c["lengths"] = list(w.lengths)
@@ -352,6 +359,16 @@ class Problem:
                                   dtype=torch.uint8)
             self._fa = fa
             return
+        if w.layout == "fp8":
+            from exact_attention_48_gb300.inputs import draw_fp8
+            q8, k8, v8, self.fp8_scales = draw_fp8(w.B, w.H, w.N, w.d, w.seed, w.input_mult, device)
+            self.inputs = [q8, k8, v8, None]
+            self.outputs = [torch.empty(q8.shape, device=device, dtype=torch.bfloat16), None, None, None]
+            self.lse_shape = (w.B, w.H, w.N)
+            self.lse = torch.empty(self.lse_shape, device=device, dtype=torch.float32)
+            self.ws = None
+            self._fa = fa
+            return
         if w.layout == "varlen":
             T = token_rows(w)
             q, k, v, do = draw_shape(1, w.H, T, w.d, w.seed, w.input_mult, device)
@@ -380,6 +397,8 @@ class Problem:
         w, fa, V = self.w, self._fa, self.view
         if w.layout == "decode":
             fa.fa_fwd_decode(q, k, v, None, w.causal, w.scale, o=o, lse=lse, workspace=self.ws)
+        elif w.layout == "fp8":
+            fa.fa_fwd_fp8(q, k, v, *self.fp8_scales, w.causal, w.scale, o=o, lse=lse)
         elif w.layout == "varlen":
             fa.fa_fwd_varlen(q, k, v, self.cu, w.N, w.causal, w.scale, o=o, lse=lse)
         elif w.layout == "bnhd":
@@ -505,13 +524,18 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
+    peak_note = "bf16"
+    if w.layout == "fp8":
+        # the 8-bit tensor path: the measured bf16 peaks times the nominal
+        # dense ratio of the two formats (4.5 / 2.25 PFLOP/s)
+        peak_sus, peak_burst, peak_note = 2.0 * peak_sus, 2.0 * peak_burst, "fp8 = 2 x bf16"
     fwd_tf = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
     bwd_tf = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12 if bwd_on else None
     # Per-kernel tensor work actually executed (the dense products of each
     # kernel, in units of the forward's 4*B*H*N^2*d): forward 1.0, dK/dV 2.0
     # (S^T, dP^T, dV, dK), dQ 1.5 (S, dP, dQ).  The backward headline keeps
     # the 2.5x count of the metric and credits no recomputation.
-    kernels = [("fa_fwd_kernel", fwd_ms, 1.0 * w.flops_fwd())]
+    kernels = [("fa_fwd_fp8_kernel" if w.layout == "fp8" else "fa_fwd_kernel", fwd_ms, 1.0 * w.flops_fwd())]
     if bwd_on:
         kernels += [("fa_bwd_dkdv_kernel", dkdv_ms, 2.0 * w.flops_fwd()),
                     ("fa_bwd_dq_kernel", dq_ms, 1.5 * w.flops_fwd())]
@@ -522,7 +546,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp8": "e4m3", "decode": "fp32"}.get(w.layout, "bf16"), "data": "synthetic",
         "config": config_of(w),
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_sustained": fwd_tf / peak_sus,
                 "frac_of_burst": fwd_tf / peak_burst},
@@ -532,7 +557,8 @@ def run_ours(args):
                            "frac_of_sustained": fl / (ms * 1e-3) / 1e12 / peak_sus} for name, ms, fl in kernels},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": dom_tf,
                      "peak": peak_sus, "unit": "TFLOP/s", "frac": dom_tf / peak_sus,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "peak_source": (f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"
+                                     + (", x2 for the fp8 path (nominal fp8/bf16 ratio)" if w.layout == "fp8" else "")),
                      "flops_per_launch": dom_flops, "traffic": traffic},
         "gpu_launches": (4 if bwd_on else 1) * args.steps,  # fwd; bwd pre, dK/dV, dQ
         "clocks": clk,
@@ -575,11 +601,11 @@ def e2e_leg(pb, args, world):
     w = pb.w
     q = pb.inputs[0]
     hq, hk, hv, hdo = (None if t is None else t.cpu().pin_memory() for t in pb.inputs)
-    outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4)]
+    outs = [torch.empty(pb.outputs[0].shape, dtype=pb.outputs[0].dtype).pin_memory() for _ in range(4)]
     hlse = torch.empty(pb.lse_shape, dtype=torch.float32).pin_memory()
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     q_, k_, v_, do_ = (None if t is None else torch.empty_like(t) for t in pb.inputs)
-    o_ = torch.empty_like(q)
+    o_ = torch.empty_like(pb.outputs[0])
     lse_ = torch.empty(pb.lse_shape, device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 20))
@@ -606,7 +632,7 @@ def e2e_leg(pb, args, world):
     torch.cuda.synchronize()
     flops = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
     value, ms = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
-    nbytes = q.numel() * q.element_size()
+    nbytes = pb.outputs[0].numel() * pb.outputs[0].element_size()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)[:n_in])
     return {"value": value, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n_out * nbytes + hlse.numel() * 4,

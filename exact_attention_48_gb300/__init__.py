@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     fa_device_status,
     fa_fwd,
     fa_fwd_decode,
+    fa_fwd_fp8,
     fa_fwd_strided,
     fa_fwd_varlen,
     library,

@@ -74,6 +74,8 @@ def library(path: str | None = None):
             lib.fa_bwd_varlen.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, p64, vp, p64,
                                           vp, p64, vp, i, i, i, i, i, i, f, vp, sz, vp]
             lib.fa_bwd_varlen.restype = i
+            lib.fa_fwd_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, i, f, vp]
+            lib.fa_fwd_fp8.restype = i
             lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.fa_decode_workspace_bytes.restype = sz
             lib.fa_fwd_decode.argtypes = [vp, p64, vp, p64, vp, p64, vp, p64, vp, vp, i, i, i, i, i, i, f, vp, sz,
@@ -261,6 +263,44 @@ def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bo
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def _check_e4m3(name, t, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError(f"{name} must hold e4m3 codes (float8_e4m3fn or uint8), got {t.dtype}")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def fa_fwd_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, causal: bool = False,
+               scale: float | None = None, o=None, lse=None, stream=None):
+    """FP8 forward: q8, k8, v8 contiguous [B, H, N, d] e4m3 codes
+    (torch.float8_e4m3fn or uint8) with one scale per tensor (value = code *
+    scale); d = 128.  Returns (o [B, H, N, d] bf16, lse [B, H, N] fp32)."""
+    _check_e4m3("q8", q8)
+    B, H, N, d = q8.shape
+    _check_e4m3("k8", k8, q8.shape)
+    _check_e4m3("v8", v8, q8.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty(q8.shape, device=q8.device, dtype=torch.bfloat16)
+    else:
+        _check_qkv("o", o, q8.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    rc = library().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), float(q_scale), float(k_scale),
+                              float(v_scale), o.data_ptr(), lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                              float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+    return o, lse
 
 
 def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:

@@ -51,6 +51,23 @@ bool encode_map(CUtensorMap *map, const void *base, int B, int H, int N, int d, 
   return r == CUDA_SUCCESS;
 }
 
+// An [B, H, N, d] e4m3 tensor (one byte per element, element strides s)
+// as 4-D (d, N, H, B); one box is a whole 128-byte row x 128 rows of one
+// head, 128-byte swizzle.  Rows past N read as 0.
+bool encode_map_u8(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n), static_cast<cuuint64_t>(s.h), static_cast<cuuint64_t>(s.b)};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 Strides contiguous(int H, int N, int d) {
   return Strides{static_cast<long long>(H) * N * d, static_cast<long long>(N) * d, d};
 }
@@ -343,6 +360,47 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   return rc;
 }
 
+// ------------------------------------------------------------------ FP8 forward
+
+fa_status_t fwd_fp8_impl(const void *q8, const void *k8, const void *v8, float sq, float sk, float sv, void *o,
+                         float *lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream) {
+  fa_status_t st = check_common(B, H, N, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(sq) || !std::isfinite(sk) || !std::isfinite(sv)) return FA_ERR_INVALID_ARGUMENT;
+  const void *ptrs[5] = {q8, k8, v8, o, lse};
+  for (const void *x : ptrs)
+    if (!x || !aligned16(x)) return FA_ERR_INVALID_ARGUMENT;
+  const size_t n8 = static_cast<size_t>(B) * H * N * d;  // bytes of each e4m3 input
+  const uintptr_t olo = reinterpret_cast<uintptr_t>(o), ohi = olo + 2 * n8;
+  const uintptr_t llo = reinterpret_cast<uintptr_t>(lse), lhi = llo + static_cast<size_t>(B) * H * N * 4;
+  const void *ins[3] = {q8, k8, v8};
+  for (const void *x : ins) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(x), hi = lo + n8;
+    if (spans_overlap(lo, hi, olo, ohi) || spans_overlap(lo, hi, llo, lhi)) return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (spans_overlap(olo, ohi, llo, lhi)) return FA_ERR_INVALID_ARGUMENT;
+  const Strides s = contiguous(H, N, d);
+  CUtensorMap tq, tk, tv;
+  if (!encode_map_u8(&tq, q8, B, H, N, d, s) || !encode_map_u8(&tk, k8, B, H, N, d, s) ||
+      !encode_map_u8(&tv, v8, B, H, N, d, s))
+    return FA_ERR_CUDA;
+  Fp8FwdParams p{};
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.so = s;
+  p.H = H;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.N = N;
+  p.BH = B * H;
+  p.num_qblk = (N + 255) / 256;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * sq * sk * 1.4426950408889634);
+  p.v_scale = sv;
+  p.neg = p.scale_log2 < 0.0f ? 1 : 0;
+  return launch_fwd_fp8(causal != 0, tq, tk, tv, p, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ decode
 
 constexpr int kDecodeMaxNq = 8;
@@ -600,6 +658,12 @@ fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const void *k
     if (!normalise_packed(in[i], H, T, d, &s[i])) return FA_ERR_INVALID_ARGUMENT;
   return bwd_impl(q, s[0], k, s[1], v, s[2], o, s[3], dO, s[4], lse, dq, s[5], dk, s[6], dv, s[7],
                   RowAxis{B, max_seqlen, cu_seqlens, T}, H, d, causal, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, float q_scale, float k_scale,
+                       float v_scale, void *o, float *lse, int B, int H, int N, int d, int causal, float scale,
+                       cudaStream_t stream) {
+  return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, causal, scale, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {

@@ -120,6 +120,24 @@ struct DecodeParams {
 cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                           cudaStream_t stream);
 
+// FP8 forward (e4m3 Q, K, V with tensor scales; d = 128).
+struct Fp8FwdParams {
+  __nv_bfloat16 *o;   // [B, H, N, d] with strides so
+  float *lse;         // [B, H, N] contiguous
+  Strides so;
+  int H;
+  int *status;
+  int N;
+  int BH;
+  int num_qblk;       // ceil(N / 256)
+  float scale_log2;   // scale * q_scale * k_scale * log2(e)
+  float v_scale;
+  int neg;            // scale_log2 < 0
+};
+
+cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const Fp8FwdParams &p, cudaStream_t stream);
+
 // Tensor maps over [B, H, N, d] bf16 tensors viewed as 4-D (d, N, H, B)
 // with the tensors' strides, box (64, 128, 1, 1), 128-byte swizzle.
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -283,6 +283,28 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// The same two products for 8-bit operands (kind::f8f6f4: e4m3 A and B
+// here, fp32 D).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   start : shared address of the first element (atoms 1024-byte aligned;
 //           a K offset inside one 128-byte row may be added to it)
@@ -321,6 +343,34 @@ __host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return static_cast
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0)
+// and fp32 D; same fields as idesc_bf16 otherwise.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two fp32 values rounded to e4m3 (nearest, ties to even, saturated to the
+// finite range) and packed: lo in the low byte, hi in the high byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// acc.x += the e4m3 value in the low byte of b, acc.y += the high byte's
+// (decoded exactly through f16, added with one rounding each).
+__device__ __forceinline__ float2 add_e4m3x2_f32(float2 acc, uint16_t b) {
+  asm("{\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, %2;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\t"
+      "add.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "h"(b));
+  return acc;
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane

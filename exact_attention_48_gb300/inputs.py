@@ -30,7 +30,7 @@ class Workload:
     seed: int = 1000
     note: str = field(default="", compare=False)
     layout: str = "bhnd"      # "bhnd" contiguous, "bnhd" ([B, N, H, d] storage), "varlen" (packed sequences),
-                              # "decode" (nq query rows against a cache of N keys)
+                              # "decode" (nq query rows against a cache of N keys), "fp8" (e4m3 inputs)
     lengths: tuple = ()       # varlen: the B sequence lengths (N is the longest)
     nq: int = 0               # decode: query rows per head
 
@@ -93,6 +93,10 @@ _VL = varlen_lengths(16384, 256, 4096, 1006)
 VARLEN_T16384H16D128 = Workload("varlen_t16384h16d128_causal", len(_VL), 16, max(_VL), 128, True, True, 1.0,
                                 1006, "packed sequences of 256..4096 tokens", layout="varlen", lengths=_VL)
 
+# The headline shape in FP8 (e4m3 Q, K, V with per-tensor scales), forward.
+FP8_B2H16N8192D128 = Workload("fp8_b2h16n8192d128", 2, 16, 8192, 128, False, False, 1.0, 1008,
+                              "headline shape, e4m3 inputs", layout="fp8")
+
 # Decoding one token per sequence against a 16384-token key/value cache
 # (bf16, contiguous [B, H, N, d] cache): HBM-bound, 2 GiB of cache per step.
 DECODE_B16H16NK16384D128 = Workload("decode_b16h16nk16384d128", 16, 16, 16384, 128, False, False, 1.0, 1007,
@@ -125,3 +129,27 @@ def draw_shape(B, H, N, d, seed, input_mult=1.0, device="cpu", dtype=torch.bfloa
     if not with_dout:
         out.append(None)
     return tuple(out)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 quantisation of an fp32 tensor for the FP8 inputs:
+    scale = amax / 448 (the format's largest finite value), codes = x /
+    scale rounded by PyTorch's float8_e4m3fn conversion.  Returns (codes,
+    scale)."""
+    amax = float(x.abs().max())
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return (x / scale).to(torch.float8_e4m3fn), scale
+
+
+def draw_fp8(B, H, N, d, seed, input_mult=1.0, device="cpu"):
+    """(q8, k8, v8, (sq, sk, sv)): N(0,1) * input_mult drawn in the order q,
+    k, v from a generator seeded with ``seed``, each quantised per tensor."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out, scales = [], []
+    for _ in range(3):
+        x = torch.randn((B, H, N, d), generator=g, device=device, dtype=torch.float32) * input_mult
+        c, s = quantize_e4m3(x)
+        out.append(c)
+        scales.append(s)
+    return out[0], out[1], out[2], tuple(scales)

@@ -178,6 +178,34 @@ FA_API fa_status_t fa_bwd_varlen(const void *q, const int64_t *q_strides, const 
                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * FP8 forward: the forward pass with Q, K, V given as e4m3 codes (OCP FP8
+ * E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, 0x7F/0xFF NaN) and one fp32 scale per tensor: element value =
+ * decoded code * q_scale (k_scale, v_scale).  Both products run on the
+ * tensor core's 8-bit path.  The page "FlashAttention-2 (DE)", section
+ * "Vergleich mit nachfolgenden Versionen" / "FlashAttention-3", names
+ * low-precision FP8 as a FlashAttention-3 addition without a formula; what
+ * this call computes, per row i (log2 units, x_ij = scale * log2(e) *
+ * q_i . k_j on the decoded, scaled values, masked keys excluded):
+ *   M_i = ceil(max_j x_ij);  w_ij = e4m3 rounding (nearest, ties to even)
+ *   of 2^(x_ij - M_i + 8), at most 256;
+ *   o_i = sum_j w_ij v_j / sum_j w_ij  (bf16);
+ *   lse_i = ln 2 * (M_i - 8 + log2 sum_j 2^(x_ij - M_i + 8))  (fp32, exact
+ *   logsumexp of the scaled scores, as in fa_fwd).
+ * The weights are what an FP8 tensor-core product of P and V can apply; the
+ * integer M_i makes them independent of how the keys are tiled (outside
+ * e4m3's subnormal range, 2^(x - M + 8) < 2^-6, where the rounding grid of
+ * a tiled pass may be finer).
+ *   q8, k8, v8 : [B, H, N, d] e4m3 codes (1 byte each), contiguous
+ *   o          : [B, H, N, d] bf16, lse : [B, H, N] fp32, contiguous
+ *   d must be 128 (FA_ERR_UNSUPPORTED otherwise); the tensor scales must
+ *   be finite; other conventions as above.
+ */
+FA_API fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, float q_scale,
+                              float k_scale, float v_scale, void *o, float *lse, int B, int H, int N,
+                              int d, int causal, float scale, cudaStream_t stream);
+
+/*
  * Decode forward: Nq new query rows per (batch entry, head) against a cache
  * of keys and values, as in token-by-token generation.  The computation is
  * the forward pass above (o and lse, same definition and scale), with

@@ -214,3 +214,20 @@ def test_decode_rejects(lib):
         assert call(ws=FAKE + (20 << 30), ws_bytes=need - 1) == FA_ERR_WORKSPACE
         assert call(ws=FAKE + (20 << 30) + 16, ws_bytes=need) == FA_ERR_INVALID_ARGUMENT
         assert call(ws=FAKE + (1 << 30), ws_bytes=need) == FA_ERR_INVALID_ARGUMENT    # workspace inside k
+
+
+def test_fp8_rejects(lib):
+    def call(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), o=FAKE + (3 << 30), lse=FAKE + (4 << 30),
+             sq=0.01, sk=0.01, sv=0.01, B=1, H=2, N=256, d=128, causal=0, scale=0.088):
+        return lib.fa_fwd_fp8(q, k, v, sq, sk, sv, o, lse, B, H, N, d, causal, scale, None)
+    assert call(d=64) == FA_ERR_UNSUPPORTED
+    assert call(d=96) == FA_ERR_UNSUPPORTED
+    assert call(N=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(causal=3) == FA_ERR_INVALID_ARGUMENT
+    assert call(sq=float("inf")) == FA_ERR_INVALID_ARGUMENT
+    assert call(sv=float("nan")) == FA_ERR_INVALID_ARGUMENT
+    assert call(scale=float("nan")) == FA_ERR_INVALID_ARGUMENT
+    assert call(k=0) == FA_ERR_INVALID_ARGUMENT
+    assert call(v=FAKE + (2 << 30) + 8) == FA_ERR_INVALID_ARGUMENT          # misaligned
+    assert call(o=FAKE + 1024) == FA_ERR_INVALID_ARGUMENT                    # o overlaps q
+    assert call(lse=FAKE + (3 << 30) + 4096) == FA_ERR_INVALID_ARGUMENT      # lse inside o
