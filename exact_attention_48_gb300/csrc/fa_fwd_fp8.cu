@@ -8,9 +8,9 @@
 // e4m3.  What the kernel computes (the oracle writes the same definition
 // out): scores from the decoded inputs times the tensor scales, in fp32;
 // the running row maximum kept as an INTEGER (log2 units), so that every
-// correction factor is an exact power of two and each weight
-// P = 2^(t - m + 8) is rounded to e4m3 on a grid that does not depend on
-// the order the key blocks are visited in; O normalised by the sum of the
+// correction factor is an exact power of two and each weight, a power of
+// two times 2^t, is rounded to e4m3 on a grid that does not depend on the
+// order the key blocks are visited in (in e4m3's normal range); O normalised by the sum of the
 // rounded weights (the weights actually applied); the logsumexp from the
 // fp32 weights before rounding.
 //
@@ -35,6 +35,10 @@ constexpr int kBN = 128;
 constexpr int kD = 128;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kTmemCols = 512;
+// The running (integer) maximum may lag a row's true maximum by up to
+// kStale (log2 units) before O is rescaled; weights are 2^(t - m + 8 - kStale)
+// <= 2^8, inside e4m3's range, and rescales become rare.
+constexpr int kStale = 2;
 constexpr int kThreads = 384;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr uint32_t kRegsLaunch = 168, kRegsControl = 104, kRegsSoftmax = 200;
@@ -126,16 +130,20 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
       }
       mx = neg ? fminf(fminf(mq[0], mq[1]), fminf(mq[2], mq[3])) : fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
     }
-    // Integer running maximum: every weight 2^(t - m + 8) is at most 256,
-    // inside e4m3's range, and a correction 2^(m_old - m_new) is exact.
-    const float m_cand = ceilf(mx * c);
-    const bool grow = m_cand > m_run;
+    // Integer running maximum m, moved to ceil(block max) only when the
+    // block max exceeds it by more than kStale: every weight
+    // 2^(t - m + 8 - kStale) is at most 256, inside e4m3's range, and a
+    // correction 2^(m_old - m_new) is exact.
+    const float t_max = mx * c;
+    const bool grow = t_max > m_run + static_cast<float>(kStale);
     float alpha = 1.0f;
     if (grow) {
-      alpha = exp2_int(m_run - m_cand);
-      m_run = m_cand;
+      const float m_new = ceilf(t_max);
+      alpha = exp2_int(m_run - m_new);
+      m_run = m_new;
     }
-    const float2 cc = make_float2(c, c), bias = make_float2(8.0f - m_run, 8.0f - m_run);
+    const float b0 = static_cast<float>(8 - kStale) - m_run;
+    const float2 cc = make_float2(c, c), bias = make_float2(b0, b0);
 
     // P as e4m3, four per 32-bit column over the first 32 columns of S; the
     // fp32 sum of the unrounded P on the way (for the logsumexp).
@@ -222,7 +230,9 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
       }
     }
-    if (store) p.lse[static_cast<long long>(bh) * N + grow_row] = (m_run - 8.0f + log2f(l_run)) * kLn2;
+    if (store)
+      p.lse[static_cast<long long>(bh) * N + grow_row] =
+          (m_run - static_cast<float>(8 - kStale) + log2f(l_run)) * kLn2;
   }
 }
 

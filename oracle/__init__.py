@@ -57,7 +57,7 @@ def _bind(path: str):
     lib.e4m3_value.restype = D
     lib.e4m3_round.argtypes = [D]
     lib.e4m3_round.restype = D
-    lib.oracle_fwd_fp8.argtypes = [u8, u8, u8, D, D, D, dp, dp, dp, L, L, L, L, I, D, D, I]
+    lib.oracle_fwd_fp8.argtypes = [u8, u8, u8, D, D, D, dp, dp, dp, L, L, L, L, I, D, D, I, I]
     lib.oracle_fwd_fp8.restype = I
     return lib
 
@@ -188,7 +188,7 @@ def _u8(x) -> np.ndarray:
 
 
 def fwd_fp8(q8, k8, v8, sq: float, sk: float, sv: float, causal: bool, scale: float, acc_rel: float = 0.0,
-            with_bound: bool = False, nthreads: int | None = None, lib=None):
+            with_bound: bool = False, stale: int = 0, nthreads: int | None = None, lib=None):
     """FP8 forward (the definition in attn_oracle.c): e4m3 codes [..., N, d]
     (uint8 arrays or float8_e4m3fn tensors) and tensor scales.  Returns
     (o, lse) in fp64, and the per-element bound when with_bound."""
@@ -203,7 +203,7 @@ def fwd_fp8(q8, k8, v8, sq: float, sk: float, sv: float, causal: bool, scale: fl
     rc = (lib or _load()).oracle_fwd_fp8(q.ctypes.data_as(u8p), k.ctypes.data_as(u8p), v.ctypes.data_as(u8p),
                                          float(sq), float(sk), float(sv), _ptr(o), _ptr(lse),
                                          _ptr(bound) if with_bound else None, BH, Nq, Nk, d,
-                                         int(bool(causal)), float(scale), float(acc_rel),
+                                         int(bool(causal)), float(scale), float(acc_rel), int(stale),
                                          nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_fp8 failed ({rc})")

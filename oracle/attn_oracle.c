@@ -431,6 +431,7 @@ typedef struct {
     int causal;
     double scale;
     double acc_rel;     /* relative precision assumed for the GPU's fp32 score sums */
+    int stale;          /* binades by which the GPU's running maximum may lag the row maximum */
     long rows_per_item, items_per_head, next_item;
     pthread_mutex_t mu;
 } fp8_job_t;
@@ -497,14 +498,15 @@ static void *fp8_worker(void *arg)
                  * scores (error <= acc_rel * |c| * sum|q k| + 2^-23 |x|) and
                  * exp2 in fp32 (relative 2^-21): if y lies that close to a
                  * rounding midpoint, its rounding may go the other way (one
-                 * ulp).  Below the normal range (one binade of margin for
-                 * the GPU's maximum), the GPU rounds on a grid that depends
-                 * on its running maximum: at most one subnormal step. */
+                 * ulp).  Below the normal range (shifted up by the lag
+                 * `stale` its running maximum may have, plus one binade of
+                 * margin), the GPU rounds on a grid that depends on that
+                 * maximum: at most one subnormal step of the GPU's scale. */
                 double dx = J->acc_rel * dw[j] + ldexp(fabs(x[j]), -23);
                 double rel = 0.6931471805599453 * dx + ldexp(1.0, -21);
                 double delta = 0.0;
-                if (y < ldexp(1.0, -5)) {
-                    delta = ldexp(1.0, -9);
+                if (y < ldexp(1.0, -5 + J->stale)) {
+                    delta = ldexp(1.0, -9 + J->stale);
                 } else {
                     int ex;
                     frexp(y, &ex);
@@ -542,11 +544,12 @@ static void *fp8_worker(void *arg)
  * scales sq, sk, sv: o[BH][Nq][d], lse[BH][Nq] (may be NULL) as defined
  * above, and optionally bound[BH][Nq][d]: how far a GPU result may lie from
  * o because of the weights whose rounding the GPU may take differently
- * (acc_rel = relative precision of the GPU's fp32 score sums). */
+ * (acc_rel = relative precision of the GPU's fp32 score sums; stale = how
+ * many binades its running maximum may lag the row maximum). */
 int oracle_fwd_fp8(const unsigned char *q8, const unsigned char *k8, const unsigned char *v8,
                    double sq, double sk, double sv, double *o, double *lse, double *bound,
                    long BH, long Nq, long Nk, long d, int causal, double scale, double acc_rel,
-                   int nthreads)
+                   int stale, int nthreads)
 {
     if (check_args(BH, Nq, Nk, d, causal) || !q8 || !k8 || !v8 || !o) return -1;
     fp8_job_t J;
@@ -555,7 +558,7 @@ int oracle_fwd_fp8(const unsigned char *q8, const unsigned char *k8, const unsig
     J.sq = sq; J.sk = sk; J.sv = sv;
     J.o = o; J.lse = lse; J.bound = bound;
     J.BH = BH; J.Nq = Nq; J.Nk = Nk; J.d = d;
-    J.causal = causal; J.scale = scale; J.acc_rel = acc_rel;
+    J.causal = causal; J.scale = scale; J.acc_rel = acc_rel; J.stale = stale < 0 ? 0 : stale;
     long want = (long)(nthreads > 0 ? nthreads : 1) * 4;
     long per_head = (want + BH - 1) / BH;
     if (per_head < 1) per_head = 1;

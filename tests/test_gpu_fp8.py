@@ -23,6 +23,7 @@ from parity import bf16_ulp, to_np
 pytestmark = pytest.mark.gpu
 
 ACC_REL = 2.0 ** -13  # relative precision assumed for the tensor core's fp32 score sums
+STALE = 2             # binades by which the kernel's running maximum may lag a row's maximum
 
 
 def _dec(x8, s):
@@ -37,7 +38,7 @@ def _check(q8, k8, v8, scales, o, lse, causal, scale, what, heads=None):
     vmax = float(v8.float().abs().max()) * sv
     for hh in (heads if heads is not None else range(B * H)):
         o_ref, lse_ref, bound = oracle.fwd_fp8(qf[hh], kf[hh], vf[hh], sq, sk, sv, causal, scale, acc_rel=ACC_REL,
-                                               with_bound=True)
+                                               with_bound=True, stale=STALE)
         og = to_np(of[hh])
         assert np.all(np.isfinite(og)), f"{what} head {hh}: non-finite O"
         err = np.abs(og - o_ref)
