@@ -192,7 +192,27 @@ def oracle_decode_sample(w, heads, target_s, nthreads=None):
     return dt, calls * 4.0 * heads * w.nq * w.N * w.d, nt, calls
 
 
+def oracle_fp8_sample(w, rows, nthreads=None):
+    """Time the oracle's FP8 forward on `rows` query rows of head (0, 0)
+    against all N keys.  Returns (seconds, flops, threads)."""
+    import oracle
+    from exact_attention_48_gb300.inputs import draw_fp8
+    q8, k8, v8, sc = draw_fp8(1, 1, w.N, w.d, w.seed, w.input_mult, "cpu")
+    nt = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.fwd_fp8(q8[0, 0, :rows], k8[0, 0], v8[0, 0], *sc, False, w.scale, nthreads=nt)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * rows * w.N * w.d, nt
+
+
 def cpu_baseline(w, target_s=12.0):
+    if w.layout == "fp8":
+        dt, fl, nt = oracle_fp8_sample(w, 64)
+        rows = int(min(w.N, max(64, target_s * fl / max(dt, 1e-6) / (4.0 * w.N * w.d))))
+        dt, fl, nt = oracle_fp8_sample(w, rows)
+        return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                "sample": f"FP8 forward of query rows 0..{rows - 1} of head (0,0) against all {w.N} keys, "
+                          f"d={w.d}, fp64 C oracle (e4m3 definition), {dt:.1f} s"}
     if w.layout == "decode":
         heads = min(w.B * w.H, 16)
         dt, fl, nt, calls = oracle_decode_sample(w, heads, target_s)
@@ -217,6 +237,8 @@ def run_reference(args):
     w = workload(args)
     if w.layout == "decode":
         return run_reference_decode(args, w)
+    if w.layout == "fp8":
+        return run_reference_fp8(args, w)
     # size each step so that warmup + steps take about 100 s in all
     dt, fl, nt = oracle_sample(w, 64)
     rate = fl / max(dt, 1e-6)
@@ -232,6 +254,29 @@ def run_reference(args):
     value = fl_total / t_total / 1e12
     sample = (f"per step: fwd+bwd of {rows} query rows of one head against all {w.N} keys, d={w.d}, "
               f"non-causal, fp64 C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_fp8(args, w):
+    per_step_s = max(0.5, min(10.0, 100.0 / max(1, args.steps + args.warmup)))
+    dt, fl, nt = oracle_fp8_sample(w, 32)
+    rows = int(min(w.N, max(8, per_step_s * fl / max(dt, 1e-6) / (4.0 * w.N * w.d))))
+    for _ in range(args.warmup):
+        oracle_fp8_sample(w, rows, nt)
+    t_total, fl_total = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl, _ = oracle_fp8_sample(w, rows, nt)
+        t_total += dt
+        fl_total += fl
+    value = fl_total / t_total / 1e12
+    sample = (f"per step: FP8 forward of {rows} query rows of one head against all {w.N} keys, d={w.d}, "
+              f"fp64 C oracle (e4m3 definition)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

@@ -52,15 +52,16 @@ bool encode_map(CUtensorMap *map, const void *base, int B, int H, int N, int d, 
 }
 
 // An [B, H, N, d] e4m3 tensor (one byte per element, element strides s)
-// as 4-D (d, N, H, B); one box is a whole 128-byte row x 128 rows of one
-// head, 128-byte swizzle.  Rows past N read as 0.
-bool encode_map_u8(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s) {
+// as 4-D (d, N, H, B); one box is a whole 128-byte row x box_rows rows of
+// one head, 128-byte swizzle.  Rows past N read as 0.
+bool encode_map_u8(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s,
+                   unsigned box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n), static_cast<cuuint64_t>(s.h), static_cast<cuuint64_t>(s.b)};
-  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t box[4] = {128, box_rows, 1, 1};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -382,8 +383,8 @@ fa_status_t fwd_fp8_impl(const void *q8, const void *k8, const void *v8, float s
   if (spans_overlap(olo, ohi, llo, lhi)) return FA_ERR_INVALID_ARGUMENT;
   const Strides s = contiguous(H, N, d);
   CUtensorMap tq, tk, tv;
-  if (!encode_map_u8(&tq, q8, B, H, N, d, s) || !encode_map_u8(&tk, k8, B, H, N, d, s) ||
-      !encode_map_u8(&tv, v8, B, H, N, d, s))
+  if (!encode_map_u8(&tq, q8, B, H, N, d, s, 128) || !encode_map_u8(&tk, k8, B, H, N, d, s, 128) ||
+      !encode_map_u8(&tv, v8, B, H, N, d, s, 128))
     return FA_ERR_CUDA;
   Fp8FwdParams p{};
   p.o = static_cast<__nv_bfloat16 *>(o);

@@ -10,9 +10,9 @@
 // the running row maximum kept as an INTEGER (log2 units), so that every
 // correction factor is an exact power of two and each weight, a power of
 // two times 2^t, is rounded to e4m3 on a grid that does not depend on the
-// order the key blocks are visited in (in e4m3's normal range); O normalised by the sum of the
-// rounded weights (the weights actually applied); the logsumexp from the
-// fp32 weights before rounding.
+// order the key blocks are visited in (in e4m3's normal range); O
+// normalised by the sum of the rounded weights (the weights actually
+// applied); the logsumexp from the fp32 weights before rounding.
 //
 // Structure as in the bf16 forward: one CTA owns 256 query rows (two tiles
 // of 128) of one head; warps 0..3 / 4..7 run the softmax of tile 0 / 1 (one
