@@ -61,11 +61,7 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
+__device__ __forceinline__ float warp_max(float x) { return warp_max_f32(x); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -389,6 +385,334 @@ __global__ void __launch_bounds__(D) fa_decode_combine_kernel(const DecodeParams
   }
 }
 
+// ------------------------------------------------------------------
+// Tensor-core decode for 3..8 query rows at d = 128.  From three rows on
+// the CUDA-core products above, not HBM, set the pace; here both products
+// run as tcgen05 MMAs with the 128 keys of a tile as M:
+//   S^T = K Q^T      (M = 128 keys, N = 16 query rows (padded), K = d)
+//   O^T += V^T P^T   (M = 128 = d, N = 16, K = 128 keys)
+// so the key is the TMEM lane for the scores and d is the lane for O.  Per
+// CTA: warps 0..3 own the rows (thread = key for the softmax, = d for the
+// output), warp 4 streams K and V by TMA, warp 5 issues the MMAs (one
+// thread) and owns TMEM.  The scores of the next tile are computed while
+// the softmax works on the current one (two S buffers, two P buffers).
+
+constexpr int kTcThreads = 192;
+constexpr int kTcN = 16;
+constexpr uint32_t kTcTmemCols = 64;  // S^T x 2 (16 each), O^T (16)
+constexpr float kTcRescale = 8.0f;    // a row's maximum moves only when exceeded by more than this (log2 units)
+
+struct TcLayout {
+  static constexpr int kStages = 3;
+  static constexpr int kSlabBytes = 128 * 128;         // 128 rows x 64 bf16
+  static constexpr int kTileBytes = 2 * kSlabBytes;    // K (or V) of one tile, d = 128
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kOffQ = kStages * kStageBytes;  // [16 rows x 128] bf16, K-major, 128-byte swizzle
+  static constexpr int kQBytes = 2 * kTcN * 128;
+  static constexpr int kOffP = kOffQ + kQBytes;        // P[2]: [16 rows x 128 keys] bf16, same layout
+  static constexpr int kOffRed = kOffP + 2 * kQBytes;  // row maxima [2][4 warps][16], row sums [4][16]
+  static constexpr int kOffBar = kOffRed + 3 * 4 * kTcN * 4;
+  static constexpr int kNumBars = 2 * kStages + 8 + 3;  // full, empty, s_full[2], s_free[2], p_ready[2], pv_done[2], q_ready, o_free, drain
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kSmemRequest = kSmemBytes + 1024;
+  static_assert(kSmemRequest <= 227 * 1024, "tensor-core decode layout exceeds shared memory");
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kQBytes % 1024 == 0, "swizzled operands need 1 KB alignment");
+};
+
+// Byte offset of element (r, c) in a K-major, 128-byte-swizzled bf16 tile
+// of `rows` rows and 128 columns (two 64-column slabs).
+__device__ __forceinline__ int sw128_off(int r, int c, int rows) {
+  const int within = (c & 63) * 2;
+  return (c >> 6) * rows * 128 + r * 128 + ((((within >> 4) ^ (r & 7))) << 4) + (within & 15);
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeParams p) {
+  using L = TcLayout;
+  constexpr int S = L::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
+  uint64_t *empty = full + S;
+  uint64_t *s_full = empty + S;
+  uint64_t *s_free = s_full + 2;
+  uint64_t *p_ready = s_free + 2;
+  uint64_t *pv_done = p_ready + 2;
+  uint64_t *q_ready = pv_done + 2;
+  uint64_t *o_free = q_ready + 1;
+  uint64_t *drain = o_free + 1;
+  uint8_t *sQ = smem + L::kOffQ;
+  uint8_t *sP = smem + L::kOffP;
+  float *red_max = reinterpret_cast<float *>(smem + L::kOffRed);  // [2][4][16]
+  float *red_sum = red_max + 2 * 4 * kTcN;                          // [4][16]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+  const WaitCtl ctl{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&p_ready[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(q_ready, 4);
+    mbar_init(o_free, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // the P buffers start at zero: rows past Nq are never written and must
+  // not bring NaNs into the (ignored) columns of O^T
+  for (int e = threadIdx.x; e < 2 * L::kQBytes / 16; e += kTcThreads)
+    reinterpret_cast<uint4 *>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, kTcTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int c = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
+        const DecodeItem x = decode_item(p, it);
+        for (int t = x.t0; t < x.t1; ++t) {
+          const int st = c % S;
+          if (!(ok = mbar_wait(&empty[st], ((c / S) & 1) ^ 1, ctl, kSiteKvEmpty))) break;
+          mbar_arrive_expect_tx(&full[st], L::kStageBytes);
+          uint8_t *dst = smem + st * L::kStageBytes;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            tma_load_4d(dst + s * L::kSlabBytes, &tm_k, &full[st], s * 64, t * kDecTileKeys, x.h, x.b);
+            tma_load_4d(dst + L::kTileBytes + s * L::kSlabBytes, &tm_v, &full[st], s * 64, t * kDecTileKeys, x.h,
+                        x.b);
+          }
+          ++c;
+        }
+      }
+      if (!ok)
+        for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[j % S], (j / S) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, kTcN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16(128, kTcN, true, false);
+      const uint64_t dQ = sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dP0 = sdesc_sw128(smem_addr(sP), 16, 1024);
+      const uint64_t dP1 = sdesc_sw128(smem_addr(sP + L::kQBytes), 16, 1024);
+      const uint32_t aStage = smem_addr(smem);
+      int c = 0, ne = 0;
+      bool ok = true;
+      // O^T += V^T P^T of global tile x (u = its index inside the item)
+      auto issue_pv = [&](int x, int u) -> bool {
+        if (!mbar_wait(&p_ready[x & 1], (x >> 1) & 1, ctl, kSitePReady)) return false;
+        tc_fence_after();
+        const uint64_t dv = sdesc_sw128(aStage + (x % S) * L::kStageBytes + L::kTileBytes, L::kSlabBytes, 1024);
+        const uint64_t dp = (x & 1) ? dP1 : dP0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 32, desc_add(dv, mnmajor_step(kk)), desc_add(dp, kmajor_step(kk, kTcN)), kIdO,
+                 (u > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&pv_done[x & 1]);
+        tc_commit(&empty[x % S]);
+        return true;
+      };
+      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
+        const DecodeItem x = decode_item(p, it);
+        const int n = x.t1 - x.t0;
+        if (n <= 0) continue;
+        if (!(ok = mbar_wait(q_ready, ne & 1, ctl, kSiteQFull))) break;
+        for (int u = 0; u < n; ++u) {
+          const int cc = c + u;
+          if (!(ok = mbar_wait(&full[cc % S], (cc / S) & 1, ctl, kSiteKvFull))) break;
+          if (!(ok = mbar_wait(&s_free[cc & 1], ((cc >> 1) & 1) ^ 1, ctl, kSiteSFull))) break;
+          tc_fence_after();
+          const uint64_t dk = sdesc_sw128(aStage + (cc % S) * L::kStageBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + (cc & 1) * kTcN, desc_add(dk, kmajor_step(kk, 128)), desc_add(dQ, kmajor_step(kk, kTcN)),
+                   kIdS, kk > 0 ? 1u : 0u);
+          tc_commit(&s_full[cc & 1]);
+          if (u == 0 && ne > 0) {  // O^T of the previous item must have been read
+            if (!(ok = mbar_wait(o_free, (ne - 1) & 1, ctl, kSiteMmaDone))) break;
+          }
+          if (u > 0 && !(ok = issue_pv(cc - 1, u - 1))) break;
+        }
+        if (!ok) break;
+        if (!(ok = issue_pv(c + n - 1, n - 1))) break;
+        c += n;
+        ++ne;
+      }
+      // every MMA issued has completed before TMEM is released
+      tc_commit(drain);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ rows
+    const int tid = threadIdx.x;  // 0..127: key of the tile (scores), d (output)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float csc = p.scale_log2;
+    int c = 0, ne = 0;
+    for (int it = blockIdx.x; it < p.items; it += gridDim.x) {
+      const DecodeItem x = decode_item(p, it);
+      const int n = x.t1 - x.t0;
+      float m[NQ], lp[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        m[q] = kNegInf;
+        lp[q] = 0.0f;
+      }
+      if (n > 0) {
+        // the item's query rows (bf16, zeros past Nq)
+        for (int e = tid; e < kTcN * 128; e += 128) {
+          const int r = e >> 7, col = e & 127;
+          __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+          if (r < p.Nq) v = p.q[row_offset(p.sq, x.bh, p.H, r) + col];
+          *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(r, col, kTcN)) = v;
+        }
+        fence_proxy_async_smem();
+        warp_arrive(q_ready);
+      }
+      const int vis_base = p.causal ? x.len - p.Nq : 0x3fffffff;
+      for (int u = 0; u < n; ++u) {
+        const int cc = c + u, b = cc & 1;
+        if (!*abort_flag) mbar_wait(&s_full[b], (cc >> 1) & 1, ctl, kSiteSFull);
+        tc_fence_after();
+        uint32_t sr[16];
+        tmem_ld16(tmem + b * kTcN + lane_base, sr);
+        tmem_ld_wait16(sr);
+        tc_fence_before();
+        warp_arrive(&s_free[b]);
+        const int j = (x.t0 + u) * kDecTileKeys + tid;  // this thread's key
+        float t[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const bool vis = q < p.Nq && j < x.len && j <= vis_base + q;
+          t[q] = vis ? __uint_as_float(sr[q]) * csc : kNegInf;
+        }
+        // tile maximum of each query row over the 128 keys
+        float *rm = red_max + b * 4 * kTcN;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const float w = warp_max_f32(t[q]);
+          if (lane == 0) rm[warp * kTcN + q] = w;
+        }
+        named_barrier(1, 128);
+        bool grow_any = false;
+        float alpha[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const float tm = fmaxf(fmaxf(rm[q], rm[kTcN + q]), fmaxf(rm[2 * kTcN + q], rm[3 * kTcN + q]));
+          alpha[q] = 1.0f;
+          if (tm > m[q] + kTcRescale || (m[q] == kNegInf && tm != kNegInf)) {
+            alpha[q] = rescale(m[q], tm);
+            m[q] = tm;
+            grow_any = true;
+          }
+        }
+        float pw[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          pw[q] = m[q] == kNegInf ? 0.0f : ex2(t[q] - m[q]);  // 0 for hidden keys
+          lp[q] = lp[q] * alpha[q] + pw[q];
+        }
+        // P buffer b is free once the P V product of tile cc - 2 is done
+        if (!*abort_flag) mbar_wait(&pv_done[b], ((cc >> 1) & 1) ^ 1, ctl, kSitePvDone);
+        uint8_t *pb = sP + b * L::kQBytes;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          *reinterpret_cast<__nv_bfloat16 *>(pb + sw128_off(q, tid, kTcN)) = __float2bfloat16_rn(pw[q]);
+        fence_proxy_async_smem();
+        if (u > 0 && grow_any) {
+          // O^T (lane = d) rescaled once the previous P V product is in
+          if (!*abort_flag) mbar_wait(&pv_done[(cc - 1) & 1], ((cc - 1) >> 1) & 1, ctl, kSitePvDone);
+          tc_fence_after();
+          uint32_t o[16];
+          tmem_ld16(tmem + 32 + lane_base, o);
+          tmem_ld_wait16(o);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
+          tmem_st16(tmem + 32 + lane_base, o);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        warp_arrive(&p_ready[b]);
+      }
+      // ---- the item's result: O^T / l, logsumexp
+      float o[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) o[q] = 0.0f;
+      if (n > 0) {
+        const int xl = c + n - 1;
+        if (!*abort_flag) mbar_wait(&pv_done[xl & 1], (xl >> 1) & 1, ctl, kSitePvDone);
+        tc_fence_after();
+        uint32_t orr[16];
+        tmem_ld16(tmem + 32 + lane_base, orr);
+        tmem_ld_wait16(orr);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) o[q] = __uint_as_float(orr[q]);
+        tc_fence_before();
+        warp_arrive(o_free);
+      }
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const float w = warp_sum(lp[q]);
+        if (lane == 0) red_sum[warp * kTcN + q] = w;
+      }
+      named_barrier(1, 128);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q >= p.Nq) break;
+        const float l = red_sum[q] + red_sum[kTcN + q] + red_sum[2 * kTcN + q] + red_sum[3 * kTcN + q];
+        const bool any = l > 0.0f;
+        const float out = any ? o[q] / l : 0.0f;
+        const float lse2 = any ? m[q] + log2f(l) : kNegInf;
+        if (p.splits == 1) {
+          p.o[row_offset(p.so, x.bh, p.H, q) + tid] = __float2bfloat16_rn(out);
+          if (tid == 0) p.lse[static_cast<long long>(x.bh) * p.Nq + q] = any ? lse2 * kLn2 : kNegInf;
+        } else {
+          const long long part = (static_cast<long long>(x.bh) * p.splits + x.split) * p.Nq + q;
+          p.part_o[part * 128 + tid] = out;
+          if (tid == 0) p.part_lse[part] = lse2;
+        }
+      }
+      named_barrier(1, 128);  // red_sum is rewritten by the next item
+      if (n > 0) {
+        c += n;
+        ++ne;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
 template <int D, int NQ>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                             cudaStream_t stream) {
@@ -403,9 +727,25 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
   return cudaGetLastError();
 }
 
+template <int NQ>
+cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
+                             cudaStream_t stream) {
+  auto kern = fa_decode_tc_kernel<NQ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout::kSmemRequest);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTcThreads, TcLayout::kSmemRequest, stream>>>(tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  fa_decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                             cudaStream_t stream) {
+  if (D == 128 && p.Nq >= 3) {  // the tensor-core products
+    return p.Nq <= 4 ? launch_decode_tc<4>(tk, tv, p, grid, stream) : launch_decode_tc<8>(tk, tv, p, grid, stream);
+  }
   if (p.Nq <= 1) return launch_decode_t<D, 1>(tk, tv, p, grid, stream);
   if (p.Nq <= 2) return launch_decode_t<D, 2>(tk, tv, p, grid, stream);
   if (p.Nq <= 4) return launch_decode_t<D, 4>(tk, tv, p, grid, stream);

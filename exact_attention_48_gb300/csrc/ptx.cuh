@@ -27,6 +27,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Maximum of x over the 32 lanes of the warp, one instruction (sm_100+);
+// every lane gets it.  Inputs are finite or -inf.
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of data).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
