@@ -36,14 +36,15 @@ EncodeTiledFn encode_fn() {
 // A [B, H, N, d] bf16 tensor with element strides s (d contiguous) viewed
 // as 4-D (d, N, H, B); one box is 64 columns (128 bytes, the swizzle span) x
 // 128 rows of one head.  Rows past N read as 0.
-bool encode_map(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s) {
+bool encode_map(CUtensorMap *map, const void *base, int B, int H, int N, int d, const Strides &s,
+                unsigned box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * 2, static_cast<cuuint64_t>(s.h) * 2,
                            static_cast<cuuint64_t>(s.b) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -527,8 +528,10 @@ fa_status_t decode_impl(const void *q, const int64_t *q_strides, const void *k, 
       if (spans_overlap(lo[i], hi[i], wlo, whi)) return FA_ERR_INVALID_ARGUMENT;
   }
 
-  CUtensorMap tk, tv;
-  if (!encode_map(&tk, k, B, H, Nk, d, sk) || !encode_map(&tv, v, B, H, Nk, d, sv)) return FA_ERR_CUDA;
+  CUtensorMap tk, tv, tq;  // q: boxes of 16 rows, the rows past Nq read as zeros
+  if (!encode_map(&tk, k, B, H, Nk, d, sk) || !encode_map(&tv, v, B, H, Nk, d, sv) ||
+      !encode_map(&tq, q, B, H, Nq, d, sq, 16))
+    return FA_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return FA_ERR_CUDA;
   void *ws = need ? workspace : nullptr;
@@ -559,7 +562,7 @@ fa_status_t decode_impl(const void *q, const int64_t *q_strides, const void *k, 
   p.scale_log2 = scale * 1.4426950408889634f;
   const int grid = p.items < sms ? p.items : sms;
   fa_status_t rc = FA_OK;
-  if (!p.status || launch_decode(d, tk, tv, p, grid, stream) != cudaSuccess) rc = FA_ERR_CUDA;
+  if (!p.status || launch_decode(d, tk, tv, tq, p, grid, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   return rc;
 }

@@ -386,33 +386,38 @@ __global__ void __launch_bounds__(D) fa_decode_combine_kernel(const DecodeParams
 }
 
 // ------------------------------------------------------------------
-// Tensor-core decode for 3..8 query rows at d = 128.  From three rows on
+// Tensor-core decode for 2..8 query rows at d = 128.  From two rows on
 // the CUDA-core products above, not HBM, set the pace; here both products
 // run as tcgen05 MMAs with the 128 keys of a tile as M:
 //   S^T = K Q^T      (M = 128 keys, N = 16 query rows (padded), K = d)
 //   O^T += V^T P^T   (M = 128 = d, N = 16, K = 128 keys)
 // so the key is the TMEM lane for the scores and d is the lane for O.  Per
-// CTA: warps 0..3 own the rows (thread = key for the softmax, = d for the
-// output), warp 4 streams K and V by TMA, warp 5 issues the MMAs (one
-// thread) and owns TMEM.  The scores of the next tile are computed while
-// the softmax works on the current one (two S buffers, two P buffers).
+// CTA: two groups of 4 row warps take alternate tiles (thread = key for the
+// softmax, = d for the output), each with its own running maxima, sums and
+// O^T accumulator, merged at the end of the item; warp 8 streams each
+// item's query rows (into one of two buffers, ahead of time) and K and V
+// by TMA; warp 9 issues the MMAs (one thread) and owns TMEM.  Each group's next
+// scores are computed while it works on the current ones (two S and two P
+// buffers per group), and the two groups' softmax chains overlap.
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;    // 8 row warps, producer, MMA issuer
 constexpr int kTcN = 16;
-constexpr uint32_t kTcTmemCols = 64;  // S^T x 2 (16 each), O^T (16)
-constexpr float kTcRescale = 8.0f;    // a row's maximum moves only when exceeded by more than this (log2 units)
+constexpr uint32_t kTcTmemCols = 128;  // per group g: S^T x 2 at 32 g (16 each), O^T at 64 + 16 g
+constexpr float kTcRescale = 8.0f;     // a row's maximum moves only when exceeded by more than this (log2 units)
 
 struct TcLayout {
   static constexpr int kStages = 3;
   static constexpr int kSlabBytes = 128 * 128;         // 128 rows x 64 bf16
   static constexpr int kTileBytes = 2 * kSlabBytes;    // K (or V) of one tile, d = 128
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kOffQ = kStages * kStageBytes;  // [16 rows x 128] bf16, K-major, 128-byte swizzle
+  static constexpr int kOffQ = kStages * kStageBytes;  // Q[2]: [16 rows x 128] bf16, K-major, 128-byte swizzle
   static constexpr int kQBytes = 2 * kTcN * 128;
-  static constexpr int kOffP = kOffQ + kQBytes;        // P[2]: [16 rows x 128 keys] bf16, same layout
-  static constexpr int kOffRed = kOffP + 2 * kQBytes;  // row maxima [2][4 warps][16], row sums [4][16]
-  static constexpr int kOffBar = kOffRed + 3 * 4 * kTcN * 4;
-  static constexpr int kNumBars = 2 * kStages + 8 + 3;  // full, empty, s_full[2], s_free[2], p_ready[2], pv_done[2], q_ready, o_free, drain
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;    // P[group][2]: [16 rows x 128 keys] bf16, same layout
+  static constexpr int kOffRed = kOffP + 4 * kQBytes;  // row maxima [group][2][4 warps][16], row sums [group][4][16]
+  static constexpr int kOffMerge = kOffRed + (2 * 2 * 4 * kTcN + 2 * 4 * kTcN) * 4;  // group 1: m[16], l[16], O^T[128][16]
+  static constexpr int kOffBar = kOffMerge + (2 * kTcN + 128 * kTcN) * 4;
+  // full[S], empty[S], per group: s_full[2], s_free[2], p_ready[2], pv_done[2], o_free; q_full[2], q_empty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 2 * 9 + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemRequest = kSmemBytes + 1024;
@@ -427,10 +432,22 @@ __device__ __forceinline__ int sw128_off(int r, int c, int rows) {
   return (c >> 6) * rows * 128 + r * 128 + ((((within >> 4) ^ (r & 7))) << 4) + (within & 15);
 }
 
+// Tiles cc = c0 .. c0+n-1 of an item alternate between the groups: tile cc
+// belongs to group cc & 1 and is that group's (cc >> 1)-th tile overall; it
+// uses the group's buffer (cc >> 1) & 1, whose k-th use is phase k >> 1.
+struct TcTile {
+  int g, b;
+  uint32_t ph;
+};
+__device__ __forceinline__ TcTile tc_tile(int cc) {
+  const int k = cc >> 1;
+  return TcTile{cc & 1, k & 1, static_cast<uint32_t>((k >> 1) & 1)};
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                        const DecodeParams p) {
+                        const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using L = TcLayout;
   constexpr int S = L::kStages;
 
@@ -438,17 +455,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
   uint64_t *empty = full + S;
-  uint64_t *s_full = empty + S;
-  uint64_t *s_free = s_full + 2;
-  uint64_t *p_ready = s_free + 2;
-  uint64_t *pv_done = p_ready + 2;
-  uint64_t *q_ready = pv_done + 2;
-  uint64_t *o_free = q_ready + 1;
-  uint64_t *drain = o_free + 1;
+  uint64_t *gb = empty + S;  // per group: [0,2) s_full, [2,4) s_free, [4,6) p_ready, [6,8) pv_done, 8 o_free
+  uint64_t *q_full = gb + 18;  // [2]
+  uint64_t *q_empty = q_full + 2;  // [2]
+  uint64_t *drain = q_empty + 2;
+  auto s_full = [&](int g, int b) { return gb + 9 * g + b; };
+  auto s_free = [&](int g, int b) { return gb + 9 * g + 2 + b; };
+  auto p_ready = [&](int g, int b) { return gb + 9 * g + 4 + b; };
+  auto pv_done = [&](int g, int b) { return gb + 9 * g + 6 + b; };
+  auto o_free = [&](int g) { return gb + 9 * g + 8; };
   uint8_t *sQ = smem + L::kOffQ;
   uint8_t *sP = smem + L::kOffP;
-  float *red_max = reinterpret_cast<float *>(smem + L::kOffRed);  // [2][4][16]
-  float *red_sum = red_max + 2 * 4 * kTcN;                          // [4][16]
+  float *red_max = reinterpret_cast<float *>(smem + L::kOffRed);  // [2][2][4][16]
+  float *red_sum = red_max + 2 * 2 * 4 * kTcN;                      // [2][4][16]
+  float *mrg = reinterpret_cast<float *>(smem + L::kOffMerge);      // m[16], l[16], O^T[128][16]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
   const WaitCtl ctl{abort_flag, p.status};
@@ -461,24 +481,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
-      mbar_init(&p_ready[b], 4);
-      mbar_init(&pv_done[b], 1);
+    for (int g = 0; g < 2; ++g) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(s_full(g, b), 1);
+        mbar_init(s_free(g, b), 4);
+        mbar_init(p_ready(g, b), 4);
+        mbar_init(pv_done(g, b), 1);
+      }
+      mbar_init(o_free(g), 4);
     }
-    mbar_init(q_ready, 4);
-    mbar_init(o_free, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   // the P buffers start at zero: rows past Nq are never written and must
   // not bring NaNs into the (ignored) columns of O^T
-  for (int e = threadIdx.x; e < 2 * L::kQBytes / 16; e += kTcThreads)
+  for (int e = threadIdx.x; e < 4 * L::kQBytes / 16; e += kTcThreads)
     reinterpret_cast<uint4 *>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kTcTmemCols);
     tmem_relinquish();
   }
@@ -487,15 +512,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int c = 0;
+      tma_prefetch_desc(&tm_q);
+      int c = 0, ne = 0;
       bool ok = true;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
         const DecodeItem x = decode_item(p, it);
+        if (x.t1 <= x.t0) continue;
+        // the item's query rows into Q buffer ne & 1 (rows past Nq read as zeros)
+        const int qb = ne & 1;
+        if (!(ok = mbar_wait(&q_empty[qb], ((ne >> 1) & 1) ^ 1, ctl, kSiteDoEmpty))) break;
+        mbar_arrive_expect_tx(&q_full[qb], L::kQBytes);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          tma_load_4d(smem + L::kOffQ + qb * L::kQBytes + s * kTcN * 128, &tm_q, &q_full[qb], s * 64, 0, x.h, x.b);
+        ++ne;
         for (int t = x.t0; t < x.t1; ++t) {
           const int st = c % S;
           if (!(ok = mbar_wait(&empty[st], ((c / S) & 1) ^ 1, ctl, kSiteKvEmpty))) break;
@@ -510,31 +545,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++c;
         }
       }
-      if (!ok)
+      if (!ok) {
         for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[j % S], (j / S) & 1);
+        for (int j = (ne > 2 ? ne - 2 : 0); j < ne; ++j) mbar_drain(&q_full[j & 1], (j >> 1) & 1);
+      }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, kTcN, false, false);
       constexpr uint32_t kIdO = idesc_bf16(128, kTcN, true, false);
-      const uint64_t dQ = sdesc_sw128(smem_addr(sQ), 16, 1024);
-      const uint64_t dP0 = sdesc_sw128(smem_addr(sP), 16, 1024);
-      const uint64_t dP1 = sdesc_sw128(smem_addr(sP + L::kQBytes), 16, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dQ1 = sdesc_sw128(smem_addr(sQ + L::kQBytes), 16, 1024);
+      const uint32_t aP = smem_addr(sP);
       const uint32_t aStage = smem_addr(smem);
       int c = 0, ne = 0;
+      int seen0 = 0, seen1 = 0;  // items in which each group has had a tile
       bool ok = true;
-      // O^T += V^T P^T of global tile x (u = its index inside the item)
-      auto issue_pv = [&](int x, int u) -> bool {
-        if (!mbar_wait(&p_ready[x & 1], (x >> 1) & 1, ctl, kSitePReady)) return false;
+      // O^T[g] += V^T P^T of global tile x; `first`: the group's first tile of the item
+      auto issue_pv = [&](int x, bool first) -> bool {
+        const TcTile tt = tc_tile(x);
+        if (!mbar_wait(p_ready(tt.g, tt.b), tt.ph, ctl, kSitePReady)) return false;
         tc_fence_after();
         const uint64_t dv = sdesc_sw128(aStage + (x % S) * L::kStageBytes + L::kTileBytes, L::kSlabBytes, 1024);
-        const uint64_t dp = (x & 1) ? dP1 : dP0;
+        const uint64_t dp = sdesc_sw128(aP + (2 * tt.g + tt.b) * L::kQBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 32, desc_add(dv, mnmajor_step(kk)), desc_add(dp, kmajor_step(kk, kTcN)), kIdO,
-                 (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&pv_done[x & 1]);
+          mma_ss(tmem + 64 + 16 * tt.g, desc_add(dv, mnmajor_step(kk)), desc_add(dp, kmajor_step(kk, kTcN)), kIdO,
+                 (!first || kk > 0) ? 1u : 0u);
+        tc_commit(pv_done(tt.g, tt.b));
         tc_commit(&empty[x % S]);
         return true;
       };
@@ -542,25 +581,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const DecodeItem x = decode_item(p, it);
         const int n = x.t1 - x.t0;
         if (n <= 0) continue;
-        if (!(ok = mbar_wait(q_ready, ne & 1, ctl, kSiteQFull))) break;
-        for (int u = 0; u < n; ++u) {
-          const int cc = c + u;
-          if (!(ok = mbar_wait(&full[cc % S], (cc / S) & 1, ctl, kSiteKvFull))) break;
-          if (!(ok = mbar_wait(&s_free[cc & 1], ((cc >> 1) & 1) ^ 1, ctl, kSiteSFull))) break;
-          tc_fence_after();
-          const uint64_t dk = sdesc_sw128(aStage + (cc % S) * L::kStageBytes, 16, 1024);
+        const int qb = ne & 1;
+        if (!(ok = mbar_wait(&q_full[qb], (ne >> 1) & 1, ctl, kSiteQFull))) break;
+        const uint64_t dQ = qb ? dQ1 : dQ0;
+        for (int u = 0; u <= n; ++u) {
+          if (u < n) {
+            const int cc = c + u;
+            const TcTile tt = tc_tile(cc);
+            if (!(ok = mbar_wait(&full[cc % S], (cc / S) & 1, ctl, kSiteKvFull))) break;
+            if (!(ok = mbar_wait(s_free(tt.g, tt.b), tt.ph ^ 1, ctl, kSiteSFull))) break;
+            tc_fence_after();
+            const uint64_t dk = sdesc_sw128(aStage + (cc % S) * L::kStageBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + (cc & 1) * kTcN, desc_add(dk, kmajor_step(kk, 128)), desc_add(dQ, kmajor_step(kk, kTcN)),
-                   kIdS, kk > 0 ? 1u : 0u);
-          tc_commit(&s_full[cc & 1]);
-          if (u == 0 && ne > 0) {  // O^T of the previous item must have been read
-            if (!(ok = mbar_wait(o_free, (ne - 1) & 1, ctl, kSiteMmaDone))) break;
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + 32 * tt.g + 16 * tt.b, desc_add(dk, kmajor_step(kk, 128)),
+                     desc_add(dQ, kmajor_step(kk, kTcN)), kIdS, kk > 0 ? 1u : 0u);
+            tc_commit(s_full(tt.g, tt.b));
+            if (u == n - 1) tc_commit(&q_empty[qb]);  // the item's last S has read its query rows
+            const int seen = tt.g ? seen1 : seen0;
+            if (u < 2 && seen > 0) {  // the group's O^T of its previous item must have been read
+              if (!(ok = mbar_wait(o_free(tt.g), (seen - 1) & 1, ctl, kSiteMmaDone))) break;
+            }
           }
-          if (u > 0 && !(ok = issue_pv(cc - 1, u - 1))) break;
+          if (u > 0 && !(ok = issue_pv(c + u - 1, u - 1 < 2))) break;
         }
         if (!ok) break;
-        if (!(ok = issue_pv(c + n - 1, n - 1))) break;
+        if (n > ((c & 1) ? 1 : 0)) ++seen0;  // group g's first tile of the item is u = (c & 1) ^ g
+        if (n > ((c & 1) ? 0 : 1)) ++seen1;
         c += n;
         ++ne;
       }
@@ -570,10 +617,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ rows
-    const int tid = threadIdx.x;  // 0..127: key of the tile (scores), d (output)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = warp >> 2;            // group
+    const int tid = threadIdx.x & 127;  // key of the tile (scores), d (output)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float csc = p.scale_log2;
-    int c = 0, ne = 0;
+    int c = 0;
     for (int it = blockIdx.x; it < p.items; it += gridDim.x) {
       const DecodeItem x = decode_item(p, it);
       const int n = x.t1 - x.t0;
@@ -583,27 +631,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m[q] = kNegInf;
         lp[q] = 0.0f;
       }
-      if (n > 0) {
-        // the item's query rows (bf16, zeros past Nq)
-        for (int e = tid; e < kTcN * 128; e += 128) {
-          const int r = e >> 7, col = e & 127;
-          __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-          if (r < p.Nq) v = p.q[row_offset(p.sq, x.bh, p.H, r) + col];
-          *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(r, col, kTcN)) = v;
-        }
-        fence_proxy_async_smem();
-        warp_arrive(q_ready);
-      }
       const int vis_base = p.causal ? x.len - p.Nq : 0x3fffffff;
-      for (int u = 0; u < n; ++u) {
-        const int cc = c + u, b = cc & 1;
-        if (!*abort_flag) mbar_wait(&s_full[b], (cc >> 1) & 1, ctl, kSiteSFull);
+      const int first_u = ((c & 1) == g) ? 0 : 1;  // this group's first tile of the item
+      int last_cc = -1;
+      for (int u = first_u; u < n; u += 2) {
+        const int cc = c + u;
+        const TcTile tt = tc_tile(cc);
+        last_cc = cc;
+        if (!*abort_flag) mbar_wait(s_full(g, tt.b), tt.ph, ctl, kSiteSFull);
         tc_fence_after();
         uint32_t sr[16];
-        tmem_ld16(tmem + b * kTcN + lane_base, sr);
+        tmem_ld16(tmem + 32 * g + 16 * tt.b + lane_base, sr);
         tmem_ld_wait16(sr);
         tc_fence_before();
-        warp_arrive(&s_free[b]);
+        warp_arrive(s_free(g, tt.b));
         const int j = (x.t0 + u) * kDecTileKeys + tid;  // this thread's key
         float t[NQ];
 #pragma unroll
@@ -612,13 +653,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           t[q] = vis ? __uint_as_float(sr[q]) * csc : kNegInf;
         }
         // tile maximum of each query row over the 128 keys
-        float *rm = red_max + b * 4 * kTcN;
+        float *rm = red_max + (g * 2 + tt.b) * 4 * kTcN;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           const float w = warp_max_f32(t[q]);
-          if (lane == 0) rm[warp * kTcN + q] = w;
+          if (lane == 0) rm[(warp & 3) * kTcN + q] = w;
         }
-        named_barrier(1, 128);
+        named_barrier(1 + g, 128);
         bool grow_any = false;
         float alpha[NQ];
 #pragma unroll
@@ -637,77 +678,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pw[q] = m[q] == kNegInf ? 0.0f : ex2(t[q] - m[q]);  // 0 for hidden keys
           lp[q] = lp[q] * alpha[q] + pw[q];
         }
-        // P buffer b is free once the P V product of tile cc - 2 is done
-        if (!*abort_flag) mbar_wait(&pv_done[b], ((cc >> 1) & 1) ^ 1, ctl, kSitePvDone);
-        uint8_t *pb = sP + b * L::kQBytes;
+        // this P buffer is free once the group's P V product two tiles back is done
+        if (!*abort_flag) mbar_wait(pv_done(g, tt.b), tt.ph ^ 1, ctl, kSitePvDone);
+        uint8_t *pb = sP + (2 * g + tt.b) * L::kQBytes;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
           *reinterpret_cast<__nv_bfloat16 *>(pb + sw128_off(q, tid, kTcN)) = __float2bfloat16_rn(pw[q]);
         fence_proxy_async_smem();
-        if (u > 0 && grow_any) {
-          // O^T (lane = d) rescaled once the previous P V product is in
-          if (!*abort_flag) mbar_wait(&pv_done[(cc - 1) & 1], ((cc - 1) >> 1) & 1, ctl, kSitePvDone);
+        if (u > first_u && grow_any) {
+          // O^T (lane = d) rescaled once the group's previous P V product is in
+          const TcTile tp = tc_tile(cc - 2);
+          if (!*abort_flag) mbar_wait(pv_done(g, tp.b), tp.ph, ctl, kSitePvDone);
           tc_fence_after();
           uint32_t o[16];
-          tmem_ld16(tmem + 32 + lane_base, o);
+          tmem_ld16(tmem + 64 + 16 * g + lane_base, o);
           tmem_ld_wait16(o);
 #pragma unroll
           for (int q = 0; q < NQ; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
-          tmem_st16(tmem + 32 + lane_base, o);
+          tmem_st16(tmem + 64 + 16 * g + lane_base, o);
           tmem_st_wait();
         }
         tc_fence_before();
-        warp_arrive(&p_ready[b]);
+        warp_arrive(p_ready(g, tt.b));
       }
-      // ---- the item's result: O^T / l, logsumexp
+      // ---- the item's result: each group's O^T, then the two merged
       float o[NQ];
 #pragma unroll
       for (int q = 0; q < NQ; ++q) o[q] = 0.0f;
-      if (n > 0) {
-        const int xl = c + n - 1;
-        if (!*abort_flag) mbar_wait(&pv_done[xl & 1], (xl >> 1) & 1, ctl, kSitePvDone);
+      if (last_cc >= 0) {
+        const TcTile tl = tc_tile(last_cc);
+        if (!*abort_flag) mbar_wait(pv_done(g, tl.b), tl.ph, ctl, kSitePvDone);
         tc_fence_after();
         uint32_t orr[16];
-        tmem_ld16(tmem + 32 + lane_base, orr);
+        tmem_ld16(tmem + 64 + 16 * g + lane_base, orr);
         tmem_ld_wait16(orr);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) o[q] = __uint_as_float(orr[q]);
         tc_fence_before();
-        warp_arrive(o_free);
+        warp_arrive(o_free(g));
       }
+      float *rs = red_sum + g * 4 * kTcN;
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         const float w = warp_sum(lp[q]);
-        if (lane == 0) red_sum[warp * kTcN + q] = w;
+        if (lane == 0) rs[(warp & 3) * kTcN + q] = w;
       }
-      named_barrier(1, 128);
+      named_barrier(1 + g, 128);
+      float l[NQ];
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        if (q >= p.Nq) break;
-        const float l = red_sum[q] + red_sum[kTcN + q] + red_sum[2 * kTcN + q] + red_sum[3 * kTcN + q];
-        const bool any = l > 0.0f;
-        const float out = any ? o[q] / l : 0.0f;
-        const float lse2 = any ? m[q] + log2f(l) : kNegInf;
-        if (p.splits == 1) {
-          p.o[row_offset(p.so, x.bh, p.H, q) + tid] = __float2bfloat16_rn(out);
-          if (tid == 0) p.lse[static_cast<long long>(x.bh) * p.Nq + q] = any ? lse2 * kLn2 : kNegInf;
-        } else {
-          const long long part = (static_cast<long long>(x.bh) * p.splits + x.split) * p.Nq + q;
-          p.part_o[part * 128 + tid] = out;
-          if (tid == 0) p.part_lse[part] = lse2;
+      for (int q = 0; q < NQ; ++q) l[q] = rs[q] + rs[kTcN + q] + rs[2 * kTcN + q] + rs[3 * kTcN + q];
+      if (g == 1) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) mrg[2 * kTcN + tid * kTcN + q] = o[q];
+        if (tid == 0) {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            mrg[q] = m[q];
+            mrg[kTcN + q] = l[q];
+          }
         }
       }
-      named_barrier(1, 128);  // red_sum is rewritten by the next item
-      if (n > 0) {
-        c += n;
-        ++ne;
+      named_barrier(3, 256);
+      if (g == 0) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (q >= p.Nq) break;
+          const float m1 = mrg[q], l1 = mrg[kTcN + q], o1 = mrg[2 * kTcN + tid * kTcN + q];
+          const float M = fmaxf(m[q], m1);
+          float lt = 0.0f, ot = 0.0f;
+          if (M != kNegInf) {
+            const float f0 = rescale(m[q], M), f1 = rescale(m1, M);
+            lt = l[q] * f0 + l1 * f1;
+            ot = (f0 > 0.0f ? o[q] * f0 : 0.0f) + (f1 > 0.0f ? o1 * f1 : 0.0f);
+          }
+          const bool any = lt > 0.0f;
+          const float out = any ? ot / lt : 0.0f;
+          const float lse2 = any ? M + log2f(lt) : kNegInf;
+          if (p.splits == 1) {
+            p.o[row_offset(p.so, x.bh, p.H, q) + tid] = __float2bfloat16_rn(out);
+            if (tid == 0) p.lse[static_cast<long long>(x.bh) * p.Nq + q] = any ? lse2 * kLn2 : kNegInf;
+          } else {
+            const long long part = (static_cast<long long>(x.bh) * p.splits + x.split) * p.Nq + q;
+            p.part_o[part * 128 + tid] = out;
+            if (tid == 0) p.part_lse[part] = lse2;
+          }
+        }
       }
+      named_barrier(3, 256);  // the merge area and the sums are rewritten by the next item
+      if (n > 0) c += n;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTcTmemCols);
   }
@@ -728,12 +792,12 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 }
 
 template <int NQ>
-cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
-                             cudaStream_t stream) {
+cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                             const DecodeParams &p, int grid, cudaStream_t stream) {
   auto kern = fa_decode_tc_kernel<NQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout::kSmemRequest);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kTcThreads, TcLayout::kSmemRequest, stream>>>(tk, tv, p);
+  kern<<<grid, kTcThreads, TcLayout::kSmemRequest, stream>>>(tk, tv, tq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   fa_decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
@@ -741,10 +805,11 @@ cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const
 }
 
 template <int D>
-cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
-                            cudaStream_t stream) {
-  if (D == 128 && p.Nq >= 3) {  // the tensor-core products
-    return p.Nq <= 4 ? launch_decode_tc<4>(tk, tv, p, grid, stream) : launch_decode_tc<8>(tk, tv, p, grid, stream);
+cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                            const DecodeParams &p, int grid, cudaStream_t stream) {
+  if (D == 128 && p.Nq >= 2) {  // the tensor-core products
+    return p.Nq <= 4 ? launch_decode_tc<4>(tk, tv, tq, p, grid, stream)
+                     : launch_decode_tc<8>(tk, tv, tq, p, grid, stream);
   }
   if (p.Nq <= 1) return launch_decode_t<D, 1>(tk, tv, p, grid, stream);
   if (p.Nq <= 2) return launch_decode_t<D, 2>(tk, tv, p, grid, stream);
@@ -754,9 +819,9 @@ cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const 
 
 }  // namespace
 
-cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
-                          cudaStream_t stream) {
-  return d == 64 ? launch_decode_d<64>(tk, tv, p, grid, stream) : launch_decode_d<128>(tk, tv, p, grid, stream);
+cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                          const DecodeParams &p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_decode_d<64>(tk, tv, tq, p, grid, stream) : launch_decode_d<128>(tk, tv, tq, p, grid, stream);
 }
 
 }  // namespace fa

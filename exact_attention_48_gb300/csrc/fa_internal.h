@@ -117,8 +117,9 @@ struct DecodeParams {
   float scale_log2;           // scale * log2(e)
 };
 
-cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
-                          cudaStream_t stream);
+// tq: q as [B, H, Nq, d] with boxes of 16 rows (used by the tensor-core kernel).
+cudaError_t launch_decode(int d, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                          const DecodeParams &p, int grid, cudaStream_t stream);
 
 // FP8 forward (e4m3 Q, K, V with tensor scales; d = 128).
 struct Fp8FwdParams {
