@@ -177,9 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
   // Tile order: causal puts the key blocks with the most query blocks
-  // (j small) first; otherwise the key blocks of one head run together.
+  // (j small) first, across all heads -- or head by head when the heaviest
+  // block is short against each SM's share of the work, so that the blocks
+  // running together share their Q and dO in L2; otherwise the key blocks
+  // of one head run together.
   int bh, jblk;
-  if (CAUSAL) {
+  if (CAUSAL && !p.head_major) {
     jblk = static_cast<int>(blockIdx.x) / p.BH;
     bh = static_cast<int>(blockIdx.x) % p.BH;
   } else {
@@ -533,9 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Tile order: causal puts the query blocks with the most key blocks
   // (i large) first; otherwise the query blocks of one head run together.
   int bh, iblk;
-  if (CAUSAL) {
+  if (CAUSAL && !p.head_major) {
     iblk = nblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
     bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else if (CAUSAL) {  // head by head, heaviest query blocks first
+    bh = static_cast<int>(blockIdx.x) / nblk;
+    iblk = nblk - 1 - static_cast<int>(blockIdx.x) % nblk;
   } else {
     bh = static_cast<int>(blockIdx.x) / nblk;
     iblk = static_cast<int>(blockIdx.x) % nblk;

@@ -95,6 +95,7 @@ struct BwdParams {
   int num_blk;                // ceil(N / 128)
   float scale;
   float scale_log2;
+  int head_major;             // causal: order the blocks head by head (heaviest first inside a head)
 };
 
 // Decode forward: Nq (<= 8) query rows per head against Nk cached keys.
