@@ -641,47 +641,107 @@ def run_ours(args):
 def e2e_leg(pb, args, world):
     """Same metric through the public API from HOST buffers: every step copies
     q, k, v, dO from pinned host memory to the device and o, lse, dq, dk, dv
-    back, inside the timed region."""
+    back, inside the timed region.
+
+    Two ways, both reported.  Sequential: copy in, compute, copy out, one
+    step after the other on one stream.  Pipelined (the value): two sets of
+    device buffers; step i's inputs are copied in on one stream while step
+    i-1 computes, and its outputs copied out on a third stream while step
+    i+1 computes, each copy ordered against the compute by events.  Every
+    step still moves all of its bytes both ways."""
     import torch
     w = pb.w
     q = pb.inputs[0]
-    hq, hk, hv, hdo = (None if t is None else t.cpu().pin_memory() for t in pb.inputs)
-    outs = [torch.empty(pb.outputs[0].shape, dtype=pb.outputs[0].dtype).pin_memory() for _ in range(4)]
-    hlse = torch.empty(pb.lse_shape, dtype=torch.float32).pin_memory()
-    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    q_, k_, v_, do_ = (None if t is None else torch.empty_like(t) for t in pb.inputs)
-    o_ = torch.empty_like(pb.outputs[0])
-    lse_ = torch.empty(pb.lse_shape, device="cuda", dtype=torch.float32)
-    stream = torch.cuda.current_stream()
-    steps = max(3, min(args.steps, 20))
     n_in, n_out = (4, 4) if w.backward else (3, 1)
+    hin = [t.cpu().pin_memory() for t in pb.inputs[:n_in]]
+    steps = max(4, min(args.steps, 20))
+    flops = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
 
-    def step():
-        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo))[:n_in]:
-            dst.copy_(src, non_blocking=True)
-        pb.fwd(q_, k_, v_, o_, lse_)
+    def make_set():
+        ins = [torch.empty_like(t) for t in pb.inputs[:n_in]]
+        outs = [torch.empty_like(pb.outputs[0])] + [torch.empty_like(q) for _ in range(n_out - 1)]
+        lse = torch.empty(pb.lse_shape, device="cuda", dtype=torch.float32)
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        hlse = torch.empty(pb.lse_shape, dtype=torch.float32).pin_memory()
+        return ins, outs, lse, hout, hlse
+
+    def compute(ins, outs, lse):
+        qq, kk, vv = ins[0], ins[1], ins[2]
+        pb.fwd(qq, kk, vv, outs[0], lse)
         if w.backward:
-            pb.bwd(q_, k_, v_, o_, do_, lse_, dq_, dk_, dv_)
-        for dst, src in zip(outs, (o_, dq_, dk_, dv_)[:n_out]):
+            pb.bwd(qq, kk, vv, outs[0], ins[3], lse, outs[1], outs[2], outs[3])
+
+    sets = [make_set(), make_set()]
+    sc = torch.cuda.current_stream()
+    sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
+
+    # sequential
+    def seq_step():
+        ins, outs, lse, hout, hlse = sets[0]
+        for dst, src in zip(ins, hin):
             dst.copy_(src, non_blocking=True)
-        hlse.copy_(lse_, non_blocking=True)
+        compute(ins, outs, lse)
+        for dst, src in zip(hout, outs):
+            dst.copy_(src, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
 
     for _ in range(2):
-        step()
+        seq_step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(sc)
     for _ in range(steps):
-        step()
-    b.record(stream)
+        seq_step()
+    b.record(sc)
     torch.cuda.synchronize()
-    flops = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
-    value, ms = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
-    nbytes = pb.outputs[0].numel() * pb.outputs[0].element_size()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)[:n_in])
-    return {"value": value, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n_out * nbytes + hlse.numel() * 4,
-            "steps": steps}
+    seq_value, _ = aggregate_throughput(flops, steps, a.elapsed_time(b), world, "cuda")
+
+    # pipelined
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
+
+    def pipe_steps(n):
+        for i in range(n):
+            bset = i & 1
+            ins, outs, lse, hout, hlse = sets[bset]
+            with torch.cuda.stream(sh):
+                if i >= 2:
+                    sh.wait_event(comp_done[bset])  # inputs of step i-2 consumed
+                for dst, src in zip(ins, hin):
+                    dst.copy_(src, non_blocking=True)
+                h2d_done[bset].record(sh)
+            sc.wait_event(h2d_done[bset])
+            if i >= 2:
+                sc.wait_event(d2h_done[bset])  # outputs of step i-2 copied out
+            compute(ins, outs, lse)
+            comp_done[bset].record(sc)
+            with torch.cuda.stream(sd):
+                sd.wait_event(comp_done[bset])
+                for dst, src in zip(hout, outs):
+                    dst.copy_(src, non_blocking=True)
+                hlse.copy_(lse, non_blocking=True)
+                d2h_done[bset].record(sd)
+        sc.wait_stream(sh)
+        sc.wait_stream(sd)
+
+    pipe_steps(2)
+    torch.cuda.synchronize()
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(sc)
+    sh.wait_stream(sc)
+    sd.wait_stream(sc)
+    pipe_steps(steps)
+    b2.record(sc)
+    torch.cuda.synchronize()
+    value, _ = aggregate_throughput(flops, steps, a2.elapsed_time(b2), world, "cuda")
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][3]) + sets[0][4].numel() * 4
+    return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "pipelined": True, "sequential_value": seq_value,
+            "note": "pipelined: each step's host->device copy overlaps the previous step's compute and its "
+                    "device->host copy the next step's, on their own streams; sequential_value: copy in, "
+                    "compute, copy out on one stream"}
 
 
 def run_sweep(args):
