@@ -156,6 +156,21 @@ def test_decode_single_chunk_path(Nq, d):
     _check(q, k, v, o, lse, [Nk] * B, False, 1.0 / math.sqrt(d), "single chunk", rows)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.3])
+@pytest.mark.parametrize("Nq,d", [(1, 128), (2, 64), (5, 128)])
+def test_decode_zero_and_negative_scale(scale, Nq, d):
+    """scale 0 gives every visible key the same weight (O is the mean of the
+    visible V rows); a negative scale favours the keys least like q.  Both
+    kernels, with causal masking and ragged cache lengths."""
+    B, H, Nk = 2, 3, 700
+    q, k, v = _draw(B, H, Nq, Nk, d, 140 + Nq + d)
+    lens = [700, 301]
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o, lse = fa_fwd_decode(q, k, v, cl, True, scale)
+    assert fa_device_status() == 0
+    _check(q, k, v, o, lse, lens, True, scale, f"scale{scale} Nq{Nq} d{d}")
+
+
 @pytest.mark.parametrize("Nq", [1, 6])
 def test_decode_deterministic(Nq):
     B, H, Nk, d = 2, 8, 20000, 128

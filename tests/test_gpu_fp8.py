@@ -50,7 +50,7 @@ def _check(q8, k8, v8, scales, o, lse, causal, scale, what, heads=None):
         assert lerr <= 1e-3, f"{what} head {hh}: LSE max err {lerr:.3e}"
 
 
-@pytest.mark.parametrize("N", [128, 200, 1000])
+@pytest.mark.parametrize("N", [1, 128, 129, 200, 1000])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_small(N, causal):
     q8, k8, v8, sc = draw_fp8(1, 2, N, 128, 50 + N, device="cuda")
@@ -74,6 +74,19 @@ def test_fp8_negative_scale_and_uint8_codes():
     o, lse = fa_fwd_fp8(q8.view(torch.uint8), k8.view(torch.uint8), v8.view(torch.uint8), *sc, False, -0.05)
     assert fa_device_status() == 0
     _check(q8, k8, v8, sc, o, lse, False, -0.05, "negative scale")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_zero_scale(causal):
+    """scale 0: every visible key gets the same weight, so O is the mean of
+    the visible rows of V and lse = log(number of visible keys)."""
+    q8, k8, v8, sc = draw_fp8(1, 2, 257, 128, 73, device="cuda")
+    o, lse = fa_fwd_fp8(q8, k8, v8, *sc, causal, 0.0)
+    assert fa_device_status() == 0
+    _check(q8, k8, v8, sc, o, lse, causal, 0.0, f"zero scale causal{int(causal)}")
+    n_vis = torch.arange(1, 258, device="cuda", dtype=torch.float32) if causal else torch.full((257,), 257.0,
+                                                                                              device="cuda")
+    assert torch.allclose(lse[0, 0], torch.log(n_vis), atol=1e-5)
 
 
 def test_fp8_close_to_exact_attention():
