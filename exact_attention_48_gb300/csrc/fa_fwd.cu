@@ -23,8 +23,12 @@
 //                normalised; the warp also owns the TMEM allocation.
 //   warps 10, 11 idle (they complete the third warpgroup).
 //
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d),
-// O_1 [256+d, 256+2d).  Only scores and probabilities of the current block
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+w),
+// O_1 [256+w, 256+2w) with w = d, except at d = 64 where w = 80: there the
+// P V product also multiplies P by a slab of ones placed after V in shared
+// memory, and O's columns 64..79 receive the sum of the bf16 weights it
+// applied (the divisor of O), which the softmax warps then need not add up
+// element by element.  Only scores and probabilities of the current block
 // ever exist, and only on chip (page "FlashAttention-2 (DE)", "Hintergrund").
 //
 // Scores are kept in the log2 domain: t = s * scale * log2(e).  The running
@@ -54,7 +58,10 @@ struct FwdLayout {
   static constexpr uint32_t kOffQ = 0;  // two tiles
   static constexpr uint32_t kOffK = kOffQ + 2 * kQTile;
   static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
+  // d = 64: one 128-key slab of bf16 ones, the extra 16 columns of V in P V
+  static constexpr uint32_t kOnesBytes = (D == 64) ? kBN * 128 : 0;
+  static constexpr uint32_t kOffOnes = kOffV + kStages * kKVBytes;
+  static constexpr uint32_t kOffBar = kOffOnes + kOnesBytes;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2], pv_done[2], drain
   static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
@@ -71,6 +78,11 @@ constexpr int kWarpProducer = 8, kWarpMma = 9;
 // (one warp of each warpgroup) 32*(104 + 2*200) <= 16384.
 constexpr uint32_t kRegsLaunch = 168, kRegsControl = 104, kRegsSoftmax = 200;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+
+// Columns of O in TMEM: d, plus 16 at d = 64 where the product also forms
+// the sum of the weights it applied.
+template <int D>
+constexpr int kOW = (D == 64) ? D + 16 : D;
 
 struct SoftmaxArgs {
   uint64_t *s_full, *p_ready, *pv_done;
@@ -197,7 +209,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
       {
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < D / 16; ++ch) {  // 16 columns at a time: P stays in registers meanwhile
+        for (int ch = 0; ch < kOW<D> / 16; ++ch) {  // 16 columns at a time: P stays in registers meanwhile
           uint32_t o[16];
           tmem_ld16(tO + ch * 16, o);
           tmem_ld_wait16(o);
@@ -212,18 +224,20 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     warp_arrive(a.p_ready);
 
     // Sum of the bf16 P the P V product used: O is divided by it, so that
-    // the weights applied to V add up to one.
-    float2 sb = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float2 sbq = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        sbq = add_bf16x2_f32(sbq, pk[q4][i]);
-      sb = fadd2(sb, sbq);
-    }
+    // the weights applied to V add up to one.  (At d = 64 the product forms
+    // it itself, in O's extra columns.)
     l_run = l_run * alpha + (sf.x + sf.y);
-    lb_run = lb_run * alpha + (sb.x + sb.y);
+    if constexpr (D != 64) {
+      float2 sb = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float2 sbq = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sbq = add_bf16x2_f32(sbq, pk[q4][i]);
+        sb = fadd2(sb, sbq);
+      }
+      lb_run = lb_run * alpha + (sb.x + sb.y);
+    }
   }
 
   // Epilogue: O / l in bf16 and the natural-log logsumexp.
@@ -233,7 +247,14 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
   }
   if (ok) {
     tc_fence_after();
-    const float inv_l = 1.0f / lb_run;
+    float lb = lb_run;
+    if constexpr (D == 64) {
+      uint32_t r16[16];
+      tmem_ld16(tO + D, r16);
+      tmem_ld_wait16(r16);
+      lb = __uint_as_float(r16[0]);
+    }
+    const float inv_l = 1.0f / lb;
     const int grow_row = a.grow0 + row;
     const bool store = grow_row < N;
     __nv_bfloat16 *orow = p.o + row_offset(p.so, bh, p.H, a.row0 + grow_row);
@@ -322,6 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (D == 64) {  // the ones slab (every bf16 1.0, so its swizzle does not matter)
+    uint4 *ones = reinterpret_cast<uint4 *>(smem + L::kOffOnes);
+    for (int i = static_cast<int>(threadIdx.x); i < static_cast<int>(L::kOnesBytes / 16); i += kThreads)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -375,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16(kBM, D, false, true);
+      constexpr uint32_t kIdescO = idesc_bf16(kBM, kOW<D>, false, true);
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-      // TMEM columns of tile t: S at t*128, O at 256 + t*D
+      // TMEM columns of tile t: S at t*128, O at 256 + t*kOW<D>
 
       // Descriptors: the Q tiles once, K/V per stage; every MMA adds a
       // compile-time step offset (the issue loops are unrolled).
@@ -398,10 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t, int j) -> bool {
         if (!mbar_wait(&p_ready[t], j & 1, ctl, kSitePReady)) return false;
         tc_fence_after();
-        const uint64_t bv = sdesc_sw128(aV + (j % S) * L::kKVBytes, kBN * 128, 1024);
+        const uint32_t aVj = aV + (j % S) * L::kKVBytes;
+        // (d = 64: the slab after V's one column slab is the ones slab)
+        const uint64_t bv = sdesc_sw128(aVj, D == 64 ? smem_addr(smem + L::kOffOnes) - aVj : kBN * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(bv, mnmajor_step(kk)), kIdescO,
+          mma_ts(tmem + 256 + t * kOW<D>, tmem + t * 128 + kk * 8, desc_add(bv, mnmajor_step(kk)), kIdescO,
                  (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[t]);
         return true;
@@ -449,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     a.p_ready = &p_ready[t];
     a.pv_done = &pv_done[t];
     a.tS = tmem + t * 128;
-    a.tO = tmem + 256 + t * D;
+    a.tO = tmem + 256 + t * kOW<D>;
     a.n_kv = t ? n1 : n0;
     a.diag = CAUSAL ? 2 * qb + t : -1;
     a.grow0 = qb * 2 * kBM + t * kBM;
