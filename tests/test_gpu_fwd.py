@@ -48,6 +48,29 @@ def test_fwd_scale_values(scale):
         check_lse(lse, lse_ref, f"scale={scale}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_rescale_every_block(d, causal):
+    """Scores that climb along the keys by about 8.5 (log2 units) per
+    128-key block: every block's maximum beats the running maximum by more
+    than the rescale threshold, so O (and at d = 64 the row sums the P V
+    product forms beside it) is rescaled at every block."""
+    N = 1000
+    scale = 1.0 / math.sqrt(d)
+    beta = 8.5 / (128 * scale * math.log2(math.e))  # score step per key, in units of q . k
+    u = torch.full((d,), 1.0 / math.sqrt(d), dtype=torch.float64)
+    q = u.expand(1, 1, N, d).clone()
+    k = (torch.arange(N, dtype=torch.float64)[:, None] * beta * u).expand(1, 1, N, d).clone()
+    g = torch.Generator().manual_seed(17)
+    v = torch.randn(1, 1, N, d, generator=g, dtype=torch.float64)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o, lse = fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    assert fa_device_status() == 0
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal, scale)
+    check_o(o, o_ref, f"ramp d={d} causal={causal}", oracle.fwd_spread(q, k, v, causal, scale))
+    check_lse(lse, lse_ref, f"ramp d={d} causal={causal}")
+
+
 def test_fwd_deterministic():
     q, k, v, _ = draw_shape(2, 4, 1000, 128, 11, 1.0, "cuda", torch.bfloat16, with_dout=False)
     o1, l1 = fa_fwd(q, k, v, True)
