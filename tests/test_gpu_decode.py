@@ -171,6 +171,27 @@ def test_decode_zero_and_negative_scale(scale, Nq, d):
     _check(q, k, v, o, lse, lens, True, scale, f"scale{scale} Nq{Nq} d{d}")
 
 
+@pytest.mark.parametrize("Nq,d", [(1, 128), (4, 128), (2, 64)])
+def test_decode_rescale_every_tile(Nq, d):
+    """Scores that climb along the cache by about 8.5 (log2 units) per
+    128-key tile: each row group's running maximum moves at every tile it
+    takes, in both kernels, and the chunks' partial results span a wide
+    range of logsumexps for the merge."""
+    B, H, Nk = 1, 2, 3000
+    scale = 1.0 / math.sqrt(d)
+    beta = 8.5 / (128 * scale * math.log2(math.e))
+    u = torch.full((d,), 1.0 / math.sqrt(d), device="cuda")
+    q = u.expand(B, H, Nq, d).to(torch.bfloat16).contiguous()
+    k = (torch.arange(Nk, device="cuda", dtype=torch.float32)[:, None] * beta * u).expand(B, H, Nk, d)
+    k = k.to(torch.bfloat16).contiguous()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(29)
+    v = torch.randn(B, H, Nk, d, generator=g, device="cuda").to(torch.bfloat16)
+    o, lse = fa_fwd_decode(q, k, v, None, True, scale)
+    assert fa_device_status() == 0
+    _check(q, k, v, o, lse, [Nk] * B, True, scale, f"ramp Nq{Nq} d{d}")
+
+
 @pytest.mark.parametrize("Nq", [1, 6])
 def test_decode_deterministic(Nq):
     B, H, Nk, d = 2, 8, 20000, 128

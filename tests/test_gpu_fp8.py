@@ -89,6 +89,26 @@ def test_fp8_zero_scale(causal):
     assert torch.allclose(lse[0, 0], torch.log(n_vis), atol=1e-5)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_rescale_every_block(causal):
+    """Scores that climb along the keys by about 4 (log2 units) per 128-key
+    block: the integer running maximum (allowed to lag by 2) moves and O is
+    rescaled at nearly every block."""
+    from exact_attention_48_gb300.inputs import quantize_e4m3
+    N, d = 1000, 128
+    scale = 1.0 / math.sqrt(d)
+    beta = 4.0 / (128 * scale * math.log2(math.e))
+    u = torch.full((d,), 1.0 / math.sqrt(d))
+    q8, sq = quantize_e4m3(u.expand(1, 1, N, d).clone())
+    k8, sk = quantize_e4m3((torch.arange(N, dtype=torch.float32)[:, None] * beta * u).expand(1, 1, N, d).clone())
+    g = torch.Generator().manual_seed(23)
+    v8, sv = quantize_e4m3(torch.randn(1, 1, N, d, generator=g))
+    q8, k8, v8 = q8.cuda(), k8.cuda(), v8.cuda()
+    o, lse = fa_fwd_fp8(q8, k8, v8, sq, sk, sv, causal, scale)
+    assert fa_device_status() == 0
+    _check(q8, k8, v8, (sq, sk, sv), o, lse, causal, scale, f"ramp causal{int(causal)}")
+
+
 def test_fp8_close_to_exact_attention():
     """Against exact attention on the decoded inputs: rounding each weight
     to e4m3 (2^-4 relative) and renormalising moves O by at most
