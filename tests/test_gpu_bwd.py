@@ -45,6 +45,34 @@ def test_bwd_small(N, d, causal):
     _check(got, ref, f"N={N} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_score_ramp(d, causal):
+    """Scores that climb along the keys by about 8.5 (log2 units) per
+    128-key block, from large queries (about 370 along one direction) and
+    keys of size at most about 1: the logsumexps reach about 75 in log2
+    units, so each recomputed weight exp2(s c - lse2) is the difference of
+    two large, nearly equal numbers.  (Keys that large instead would make dQ
+    = s dS K cancel a large common part of K, where the bf16 rounding of dS
+    alone exceeds the gradient tolerance: a property of bf16 dS, not of the
+    recomputation.)"""
+    N = 1000
+    scale = 1.0 / math.sqrt(d)
+    a = 8.5 * N / (128 * scale * math.log2(math.e))
+    u = torch.full((d,), 1.0 / math.sqrt(d), dtype=torch.float64)
+    g = torch.Generator().manual_seed(31)
+    q = (a * u + torch.randn(N, d, generator=g, dtype=torch.float64)).expand(1, 1, N, d).clone()
+    k = (torch.arange(N, dtype=torch.float64)[:, None] / N * u +
+         0.05 * torch.randn(N, d, generator=g, dtype=torch.float64)).expand(1, 1, N, d).clone()
+    v, do = (torch.randn(1, 1, N, d, generator=g, dtype=torch.float64) for _ in range(2))
+    q, k, v, do = (t.to(torch.bfloat16) for t in (q, k, v, do))
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa_fwd(qc, kc, vc, causal, scale)
+    got = fa_bwd(qc, kc, vc, o, doc, lse, causal, scale)
+    assert fa_device_status() == 0
+    _check(got, oracle.bwd(q, k, v, do, causal, scale), f"ramp d={d} causal={causal}")
+
+
 def test_bwd_caller_workspace_and_reuse():
     """A caller workspace filled with garbage gives the same result as the
     library's own allocation, and it can be reused call after call."""
