@@ -12,9 +12,12 @@
 // The array is a file-scope __device__ variable of FA_NOALLOC_SCRATCH_BYTES
 // bytes: every GPU that loads the library holds it until the process
 // exits.  In host code its name only stands in for the device object, so
-// the device address is looked up with cudaGetSymbolAddress once per
-// device, the first time fa_bwd_noalloc runs with that device current.
-// That first call should therefore come before any stream capture.
+// every call looks up the array's device address on the current device with
+// cudaGetSymbolAddress (a host-side query: it enqueues nothing).  The
+// address is not cached: after cudaDeviceReset, or under another context on
+// the same device, the module is loaded again and the array may move.  The
+// first lookup in a process may load the module, so the first call should
+// come before any stream capture.
 //
 // Every call uses the same array and leaves its last contents there.
 // Nothing in it has to start at zero: the first kernel of each call writes
@@ -22,31 +25,20 @@
 // overlaps on the GPU (different streams, or different host threads, on the
 // same device) race on the array; callers must order them.
 
+#include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/fa.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_setup_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on first use).
+// Device address of the scratch array in the current context.
 fa_status_t scratch_address(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return FA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
-  }
-  *out = g_scratch_ptr[dev];
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+  *out = ptr;
   return FA_OK;
 }
 
@@ -55,12 +47,14 @@ fa_status_t scratch_address(void **out) {
 extern "C" fa_status_t fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dO,
                                       const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
                                       int causal, float scale, cudaStream_t stream) {
-  // Host-side checks first (no CUDA call before them): pointers, then the
-  // size of the scratch the call needs.  fa_bwd_workspace_bytes returns 0
-  // for sizes fa_bwd rejects; fa_bwd reports those with its own code.
+  // Host-side checks first (no CUDA call before them): pointers, flags and
+  // scale, then the size of the scratch the call needs.
+  // fa_bwd_workspace_bytes returns 0 for sizes fa_bwd rejects; fa_bwd
+  // reports those with its own code.
   const void *ptrs[9] = {q, k, v, o, dO, lse, dq, dk, dv};
   for (const void *x : ptrs)
     if (!x || (reinterpret_cast<uintptr_t>(x) & 15u)) return FA_ERR_INVALID_ARGUMENT;
+  if ((causal != 0 && causal != 1) || !std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   if (need == 0)  // invalid sizes: let fa_bwd name the error, without touching the device
