@@ -59,6 +59,9 @@ def _bind(path: str):
     lib.e4m3_round.restype = D
     lib.oracle_fwd_fp8.argtypes = [u8, u8, u8, D, D, D, dp, dp, dp, L, L, L, L, I, D, D, I, I]
     lib.oracle_fwd_fp8.restype = I
+    lib.oracle_fwd_fp8_detail.argtypes = [u8, u8, u8, D, D, D, dp, dp, dp, L, L, L, L, I, D, D, I, I,
+                                          dp, dp, dp, dp]
+    lib.oracle_fwd_fp8_detail.restype = I
     return lib
 
 
@@ -208,3 +211,28 @@ def fwd_fp8(q8, k8, v8, sq: float, sk: float, sv: float, causal: bool, scale: fl
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_fp8 failed ({rc})")
     return (o, lse, bound) if with_bound else (o, lse)
+
+
+def fwd_fp8_detail(q8, k8, v8, sq: float, sk: float, sv: float, causal: bool, scale: float,
+                   acc_rel: float = 0.0, stale: int = 0, lib=None):
+    """fwd_fp8 with the bound, plus the per-key detail of the definition:
+    returns a dict with o, lse, bound [..., Nq, d], x (scores in log2 units,
+    -inf where masked), w (rounded weights), delta (the change of each
+    weight the bound allows) [..., Nq, Nk] and M [..., Nq].  Small cases."""
+    q, k, v = _u8(q8), _u8(k8), _u8(v8)
+    lead, BH, Nq, Nk, d = _shape(q, k)
+    if v.shape != k.shape:
+        raise ValueError("v must have the shape of k")
+    out = {"o": np.empty(q.shape, np.float64), "lse": np.empty(lead + (Nq,), np.float64),
+           "bound": np.empty(q.shape, np.float64)}
+    for name in ("x", "w", "delta"):
+        out[name] = np.empty(lead + (Nq, Nk), np.float64)
+    out["M"] = np.empty(lead + (Nq,), np.float64)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    rc = (lib or _load()).oracle_fwd_fp8_detail(
+        q.ctypes.data_as(u8p), k.ctypes.data_as(u8p), v.ctypes.data_as(u8p), float(sq), float(sk), float(sv),
+        _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["bound"]), BH, Nq, Nk, d, int(bool(causal)), float(scale),
+        float(acc_rel), int(stale), 1, _ptr(out["x"]), _ptr(out["w"]), _ptr(out["delta"]), _ptr(out["M"]))
+    if rc != 0:
+        raise RuntimeError(f"oracle_fwd_fp8_detail failed ({rc})")
+    return out

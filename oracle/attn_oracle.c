@@ -432,6 +432,7 @@ typedef struct {
     double scale;
     double acc_rel;     /* relative precision assumed for the GPU's fp32 score sums */
     int stale;          /* binades by which the GPU's running maximum may lag the row maximum */
+    double *x_out, *w_out, *delta_out, *M_out;   /* optional per-key detail: [BH][Nq][Nk], M [BH][Nq] */
     long rows_per_item, items_per_head, next_item;
     pthread_mutex_t mu;
 } fp8_job_t;
@@ -516,6 +517,16 @@ static void *fp8_worker(void *arg)
                 }
                 dw[j] = delta;
             }
+            if (J->w_out) {
+                const long base = (h * J->Nq + i) * J->Nk;
+                for (long j = 0; j < J->Nk; ++j) {
+                    const int vis = j < end;
+                    J->x_out[base + j] = vis ? x[j] : -INFINITY;
+                    J->w_out[base + j] = vis ? w[j] : 0.0;
+                    J->delta_out[base + j] = vis ? dw[j] : 0.0;
+                }
+                J->M_out[h * J->Nq + i] = M;
+            }
             double *oi = J->o + (h * J->Nq + i) * d;
             for (long cc = 0; cc < d; ++cc) {
                 double acc = 0.0;
@@ -546,14 +557,36 @@ static void *fp8_worker(void *arg)
  * o because of the weights whose rounding the GPU may take differently
  * (acc_rel = relative precision of the GPU's fp32 score sums; stale = how
  * many binades its running maximum may lag the row maximum). */
+int oracle_fwd_fp8_detail(const unsigned char *q8, const unsigned char *k8, const unsigned char *v8,
+                          double sq, double sk, double sv, double *o, double *lse, double *bound,
+                          long BH, long Nq, long Nk, long d, int causal, double scale, double acc_rel,
+                          int stale, int nthreads, double *x_out, double *w_out, double *delta_out,
+                          double *M_out);
+
 int oracle_fwd_fp8(const unsigned char *q8, const unsigned char *k8, const unsigned char *v8,
                    double sq, double sk, double sv, double *o, double *lse, double *bound,
                    long BH, long Nq, long Nk, long d, int causal, double scale, double acc_rel,
                    int stale, int nthreads)
 {
+    return oracle_fwd_fp8_detail(q8, k8, v8, sq, sk, sv, o, lse, bound, BH, Nq, Nk, d, causal, scale,
+                                 acc_rel, stale, nthreads, NULL, NULL, NULL, NULL);
+}
+
+/* The same, also returning for every (row, key) the score x (log2 units,
+ * -inf where masked), the rounded weight w and the change delta that the
+ * bound allows for it, and each row's M: x_out, w_out, delta_out
+ * [BH][Nq][Nk] and M_out [BH][Nq], all four or none.  For small tests. */
+int oracle_fwd_fp8_detail(const unsigned char *q8, const unsigned char *k8, const unsigned char *v8,
+                          double sq, double sk, double sv, double *o, double *lse, double *bound,
+                          long BH, long Nq, long Nk, long d, int causal, double scale, double acc_rel,
+                          int stale, int nthreads, double *x_out, double *w_out, double *delta_out,
+                          double *M_out)
+{
     if (check_args(BH, Nq, Nk, d, causal) || !q8 || !k8 || !v8 || !o) return -1;
+    if ((x_out || w_out || delta_out || M_out) && !(x_out && w_out && delta_out && M_out)) return -1;
     fp8_job_t J;
     memset(&J, 0, sizeof(J));
+    J.x_out = x_out; J.w_out = w_out; J.delta_out = delta_out; J.M_out = M_out;
     J.q8 = q8; J.k8 = k8; J.v8 = v8;
     J.sq = sq; J.sk = sk; J.sv = sv;
     J.o = o; J.lse = lse; J.bound = bound;

@@ -10,8 +10,17 @@ independently of that code:
   * Q = 0 gives the (prefix) mean of V with LSE = ln(count); constant V
     returns V (the rounded weights are normalised by their own sum);
   * O differs from exact attention by no more than rounding each weight to
-    e4m3 can explain (relative 2^-4 per normal weight).
+    e4m3 can explain (relative 2^-4 per normal weight);
+  * a hand-worked example (tests/golden/fp8_hand_d4.json) fixes M_i =
+    ceil(max) against floor and round: one weight in the subnormal range,
+    one maximum whose floor would saturate the largest weight;
+  * the per-element bound: it covers the worst change of the flagged
+    weights and is tight for it; every weight it leaves unflagged keeps
+    its rounding under the score error model; and a tiled pass written
+    here, whose integer running maximum lags the row maximum by up to
+    STALE binades in random patterns, stays within it.
 """
+import json
 import math
 import os
 
@@ -22,6 +31,11 @@ import torch
 import oracle
 
 F8 = torch.float8_e4m3fn
+# The tolerance model the GPU tests use: relative precision of the
+# hardware's fp32 sums of e4m3 products, and how many binades a tiled pass's
+# integer running maximum may lag the row maximum.
+ACC_REL = 2.0 ** -13
+STALE = 2
 
 
 def test_e4m3_values_match_torch(lib=None):
@@ -160,6 +174,146 @@ def test_fp8_bound_flags_nothing_for_exact_weights():
     assert np.all(b == 0.0)
 
 
+def _golden_fp8():
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "fp8_hand_d4.json")) as f:
+        return json.load(f)
+
+
+def test_fp8_hand_worked_example(lib=None):
+    """The definition evaluated by hand on two tiny heads (derivation in the
+    fixture): M = ceil(max x), e4m3 weights, normalised by their sum."""
+    g = _golden_fp8()
+    q8, k8, v8 = (torch.tensor(g[n], dtype=torch.float32).to(F8) for n in ("q", "k", "v"))
+    for n, t in (("q", q8), ("k", k8), ("v", v8)):   # the inputs are exact e4m3 values
+        assert np.array_equal(_dec(t), np.array(g[n], dtype=np.float64))
+    o, lse = oracle.fwd_fp8(q8, k8, v8, g["sq"], g["sk"], g["sv"], False, g["scale"], lib=lib)
+    np.testing.assert_allclose(o, np.array(g["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(g["lse"]), rtol=0, atol=1e-12)
+    r = oracle.fwd_fp8_detail(q8, k8, v8, g["sq"], g["sk"], g["sv"], False, g["scale"], lib=lib)
+    for h in range(2):
+        assert np.all(r["M"][h] == g["M"][h])
+        for i in range(3):
+            np.testing.assert_array_equal(r["w"][h, i], np.array(g["weights"][h]))
+
+
+def _bound_case(seed, causal, mult=2.0, N=48, d=32, acc_rel=ACC_REL, stale=STALE, lib=None):
+    q8, k8, v8 = _random_case(seed, H=2, N=N, d=d, mult=mult)
+    sq = sk = 1 / 16
+    scale = 1 / math.sqrt(d)
+    r = oracle.fwd_fp8_detail(q8, k8, v8, sq, sk, 1.0, causal, scale, acc_rel, stale, lib=lib)
+    return q8, k8, v8, sq, sk, scale, r
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_bound_covers_and_is_tight_for_worst_weight_changes(causal, lib=None):
+    """Move every flagged weight by its allowed change (delta) in the
+    direction that pushes each output element furthest, renormalise, and
+    recompute O directly: the change stays within the bound, and reaches
+    it up to the factor (W - sum delta) / (W + sum delta).  Random sign
+    patterns stay within it too."""
+    _, _, v8, _, _, _, r = _bound_case(51, causal, lib=lib)
+    v = _dec(v8)
+    w, dl, o, b = r["w"], r["delta"], r["o"], r["bound"]
+    assert (dl > 0).sum() > 20, "the case must exercise the bound"
+    rng = np.random.default_rng(5)
+    H, Nq, Nk = w.shape
+    for h in range(H):
+        for i in range(Nq):
+            flagged = dl[h, i] > 0
+            if not flagged.any():
+                assert np.all(b[h, i] == 0.0)
+                continue
+            diff = v[h] - o[h, i][None, :]                      # [Nk, d]
+            patterns = [np.sign(diff), -np.sign(diff)] + [rng.choice([-1.0, 1.0], size=diff.shape) for _ in range(4)]
+            W, S = w[h, i].sum(), dl[h, i].sum()
+            for k, eps in enumerate(patterns):
+                wp = w[h, i][:, None] + eps * dl[h, i][:, None]   # per output column
+                op = (wp * v[h]).sum(0) / wp.sum(0)
+                change = np.abs(op - o[h, i])
+                assert np.all(change <= b[h, i] * (1 + 1e-9) + 1e-15), (h, i, k)
+                if k == 0:  # the aligned pattern nearly reaches the bound
+                    assert np.all(change >= b[h, i] * (W - S) / (W + S) * (1 - 1e-9) - 1e-15), (h, i)
+
+
+def test_fp8_unflagged_weights_keep_their_rounding(lib=None):
+    """The scores recomputed here (decoded values, fp64) moved by the error
+    model -- acc_rel * |c| * sum|q k| + 2^-23 |x| on the score, 2^-21
+    relative on exp2 -- and rounded with PyTorch's float8 conversion: every
+    weight the oracle leaves unflagged in the normal band keeps its value;
+    every weight in the band below 2^(-5 + stale) is flagged with one
+    subnormal step at the lagged scale; and the oracle's weights themselves
+    are PyTorch's rounding of the exact 2^(x - M + 8)."""
+    q8, k8, v8, sq, sk, scale, r = _bound_case(52, False, mult=2.0, N=64, lib=lib)
+    q, k = sq * _dec(q8), sk * _dec(k8)
+    c = scale / math.log(2.0)
+    x = c * np.einsum("hid,hjd->hij", q, k)
+    mag = abs(c) * np.einsum("hid,hjd->hij", np.abs(q), np.abs(k))
+    M = np.ceil(x.max(-1))
+    np.testing.assert_array_equal(M, r["M"])
+    y = np.exp2(x - M[..., None] + 8.0)
+    rnd = lambda a: torch.from_numpy(np.minimum(a, 448.0)).to(F8).to(torch.float64).numpy()  # noqa: E731
+    np.testing.assert_array_equal(rnd(y), r["w"])
+    dx = ACC_REL * mag + 2.0 ** -23 * np.abs(x)
+    band = y < 2.0 ** (-5 + STALE)
+    np.testing.assert_array_equal(r["delta"][band], 2.0 ** (-9 + STALE))
+    normal_unflagged = (~band) & (r["delta"] == 0)
+    for sx in (-1.0, 1.0):
+        for se in (-1.0, 1.0):
+            yp = np.exp2(x + sx * dx - M[..., None] + 8.0) * (1.0 + se * 2.0 ** -21)
+            same = rnd(yp) == r["w"]
+            assert np.all(same[normal_unflagged]), "an unflagged weight can round the other way"
+    assert (r["delta"][~band] > 0).any(), "the case must flag some weights near a rounding midpoint"
+
+
+def _tiled_fp8_pass(x, v, lag, rng, blk=8):
+    """An FP8 forward pass over key blocks with an integer running maximum
+    m that may lag the row maximum seen so far by up to `lag` binades: the
+    weights of a block are e4m3(2^(x - m + 8 - lag)) (never above 2^8), the
+    sums of weights and of weighted values are kept in fp64 and rescaled by
+    2^(m_old - m_new) when m moves (it must once the maximum seen exceeds
+    it by more than `lag`; where it lands in the allowed range is drawn at
+    random).  x: [Nk] scores in log2 units (-inf where masked); v: [Nk, d]."""
+    to8 = lambda a: torch.from_numpy(a).to(F8).to(torch.float64).numpy()  # noqa: E731
+    m, acc, wsum, seen = None, np.zeros(v.shape[1]), 0.0, -np.inf
+    for j0 in range(0, x.shape[0], blk):
+        xb, vb = x[j0:j0 + blk], v[j0:j0 + blk]
+        if not np.isfinite(xb).any():
+            continue
+        seen = max(seen, float(np.max(xb)))
+        r = math.ceil(seen)
+        if m is None or r - m > lag:
+            m_new = r - int(rng.integers(0, lag + 1))
+            if m is not None:
+                acc, wsum = acc * 2.0 ** (m - m_new), wsum * 2.0 ** (m - m_new)
+            m = m_new
+        wb = to8(np.exp2(xb - m + 8 - lag))
+        acc = acc + wb @ vb
+        wsum += wb.sum()
+    return acc / wsum
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_tiled_pass_with_lagging_maximum_stays_within_bound(causal, lib=None):
+    """Against a tiled pass written here with random lag patterns up to
+    STALE (exact scores, so only the rounding grid differs): every output
+    element within the oracle's bound for stale = STALE (acc_rel = 0)."""
+    q8, k8, v8, sq, sk, scale, r = _bound_case(53, causal, mult=2.5, N=64, acc_rel=0.0, lib=lib)
+    q, k, v = sq * _dec(q8), sk * _dec(k8), _dec(v8)
+    x = scale / math.log(2.0) * np.einsum("hid,hjd->hij", q, k)
+    if causal:
+        x = np.where(np.tril(np.ones(x.shape[-2:], dtype=bool)), x, -np.inf)
+    rng = np.random.default_rng(9)
+    worst = 0.0
+    for h in range(x.shape[0]):
+        for i in range(x.shape[1]):
+            for _ in range(3):
+                o_t = _tiled_fp8_pass(x[h, i], v[h], STALE, rng)
+                excess = np.abs(o_t - r["o"][h, i]) - r["bound"][h, i]
+                assert np.all(excess <= 1e-13), (h, i, float(excess.max()))
+                worst = max(worst, float(np.max(np.abs(o_t - r["o"][h, i]))))
+    assert worst > 0.0, "the lag must change some roundings"
+
+
 # Plausible mistakes in the FP8 part of the oracle source; each must be
 # caught by one of the pins above (run against a mutated copy).
 FP8_PINS = [
@@ -170,6 +324,10 @@ FP8_PINS = [
     lambda lib: [test_fp8_lse_is_exact(c, lib) for c in (False, True)],
     lambda lib: [test_fp8_zero_queries_and_constant_values(c, lib) for c in (False, True)],
     lambda lib: [test_fp8_close_to_exact_within_rounding(m, lib) for m in (1.0, 2.0)],
+    lambda lib: test_fp8_hand_worked_example(lib),
+    lambda lib: [test_fp8_bound_covers_and_is_tight_for_worst_weight_changes(c, lib) for c in (False, True)],
+    lambda lib: test_fp8_unflagged_weights_keep_their_rounding(lib),
+    lambda lib: [test_fp8_tiled_pass_with_lagging_maximum_stays_within_bound(c, lib) for c in (False, True)],
 ]
 FP8_MUTATIONS = [
     ("normalise_by_unrounded_sum", "oi[cc] = J->sv * acc / W;", "oi[cc] = J->sv * acc / Z;"),
@@ -182,6 +340,13 @@ FP8_MUTATIONS = [
      "long end = J->causal ? (i < J->Nk ? i : J->Nk) : J->Nk;"),
     ("mantissa_two_bits", "double ulp = ldexp(1.0, e - 3);", "double ulp = ldexp(1.0, e - 2);"),
     ("exponent_bias_8", "else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("max_scale_floor", "double M = ceil(mx);", "double M = floor(mx);"),
+    ("max_scale_round", "double M = ceil(mx);", "double M = nearbyint(mx);"),
+    ("bound_halved", "bi[cc] = (W - dsum > 0.0) ? fabs(J->sv) * b / (W - dsum) : INFINITY;",
+     "bi[cc] = (W - dsum > 0.0) ? 0.5 * fabs(J->sv) * b / (W - dsum) : INFINITY;"),
+    ("bound_ignores_lag_band", "if (y < ldexp(1.0, -5 + J->stale)) {", "if (y < ldexp(1.0, -5)) {"),
+    ("bound_ignores_lag_step", "delta = ldexp(1.0, -9 + J->stale);", "delta = ldexp(1.0, -9);"),
+    ("bound_ignores_score_error", "if (fabs(y - mid) <= rel * y) delta = ulp;", "if (fabs(y - mid) <= 0.0 * y) delta = ulp;"),
 ]
 
 
