@@ -53,12 +53,35 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    return _build_into(BUILD, LIB, [], verbose)
+
+
+# Test builds: the same sources with extra preprocessor definitions, linked
+# into their own folder under _build/ (never into libfa.so).  The one used
+# by the tests shortens every pipeline wait to FA_WAIT_LIMIT_CYCLES and
+# leaves out the forward's first V load, so that the bounded-wait path
+# (FA_ERR_DEVICE_TIMEOUT through fa_device_status) can be exercised
+# without any kernel waiting for long.
+VARIANTS = {
+    "stalltest": ["-DFA_WAIT_LIMIT_CYCLES=2000000LL", "-DFA_TEST_SKIP_FIRST_V_LOAD"],
+}
+
+
+def build_variant(name: str, force: bool = False) -> str:
+    out_dir = os.path.join(BUILD, name)
+    lib = os.path.join(out_dir, "libfa.so")
+    if not force and os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    return _build_into(out_dir, lib, VARIANTS[name], False)
+
+
+def _build_into(out_dir: str, lib: str, defines, verbose: bool) -> str:
+    os.makedirs(out_dir, exist_ok=True)
     exe = nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + list(defines)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [exe, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -71,14 +94,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if r.returncode:
                 raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
             objs.append(obj)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [exe, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("linking libfa.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"linking {lib} failed")
+    os.replace(tmp, lib)
+    return lib
 
 
 def main():

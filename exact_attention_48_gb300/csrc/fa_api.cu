@@ -170,14 +170,23 @@ int *status_ptr() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr long long kMaxGridX = 2147483647LL;  // largest x extent of a launch grid
+
 // Host-side checks shared by both passes; no CUDA call happens before them.
 fa_status_t check_common(int B, int H, int N, int d, int causal, float scale) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARGUMENT;
   if (d != 64 && d != 128) return d < 1 ? FA_ERR_INVALID_ARGUMENT : FA_ERR_UNSUPPORTED;
-  const long long elems = static_cast<long long>(B) * H * N * d;
-  if (elems >= (1LL << 31)) return FA_ERR_INVALID_ARGUMENT;
+  // The backward launches one CTA per (head, block of 128 rows): that count
+  // must fit a grid's x extent.  Within it B*H*N < 2^38, so the element
+  // count below cannot overflow.
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * ((N + 127) / 128) > kMaxGridX) return FA_ERR_INVALID_ARGUMENT;
+  // TMA addresses a tensor with byte strides below 2^40: at most 2^39 bf16
+  // elements (1 TiB) per tensor, more than a GPU's memory holds.
+  const long long elems = bh * N * d;
+  if (elems >= (1LL << 39)) return FA_ERR_INVALID_ARGUMENT;
   return FA_OK;
 }
 

@@ -53,37 +53,42 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   // One padded row per kTpr threads: rows q < N of every head get
   // D = rowsum(dO o O) and lse * log2(e); the padding rows up to the next
   // multiple of 128 get D = 0 and lse = +inf (probability 0), so the main
-  // kernels read whole blocks without checks.
+  // kernels read whole blocks without checks.  The grid strides over the
+  // rows (block-uniform trip count, so every warp's shuffles see all lanes).
   constexpr int kTpr = D / 8;  // threads per row: 8 bf16 (16 bytes) each
   constexpr int kRowsPerBlock = 256 / kTpr;
   const int Np = p.num_blk * kBlk;
-  const long long prow = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kTpr;
-  const bool in_range = prow < static_cast<long long>(p.BH) * Np;
-  const int bh = in_range ? static_cast<int>(prow / Np) : 0;
-  const int q = in_range ? static_cast<int>(prow % Np) : 0;
-  const SeqRange seq = seq_range(p.cu_seqlens, bh / p.H, p.N, p.T);
-  const bool real = in_range && q < seq.len;
-  const int trow = seq.start + q;  // the row on the tensors' row axis
+  const long long rows = static_cast<long long>(p.BH) * Np;
   const int part = threadIdx.x % kTpr;
-  float acc = 0.0f;
-  if (real) {
-    const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row_offset(p.so, bh, p.H, trow))[part];
-    const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row_offset(p.sdo, bh, p.H, trow))[part];
-    const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
-    const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
+  for (long long base = static_cast<long long>(blockIdx.x) * kRowsPerBlock; base < rows;
+       base += static_cast<long long>(gridDim.x) * kRowsPerBlock) {
+    const long long prow = base + threadIdx.x / kTpr;
+    const bool in_range = prow < rows;
+    const int bh = in_range ? static_cast<int>(prow / Np) : 0;
+    const int q = in_range ? static_cast<int>(prow % Np) : 0;
+    const SeqRange seq = seq_range(p.cu_seqlens, bh / p.H, p.N, p.T);
+    const bool real = in_range && q < seq.len;
+    const int trow = seq.start + q;  // the row on the tensors' row axis
+    float acc = 0.0f;
+    if (real) {
+      const uint4 ov = reinterpret_cast<const uint4 *>(p.o + row_offset(p.so, bh, p.H, trow))[part];
+      const uint4 dv = reinterpret_cast<const uint4 *>(p.dout + row_offset(p.sdo, bh, p.H, trow))[part];
+      const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+      const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = __bfloat1622float2(o2[i]);
-      const float2 b = __bfloat1622float2(d2[i]);
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(o2[i]);
+        const float2 b = __bfloat1622float2(d2[i]);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+      }
     }
-  }
 #pragma unroll
-  for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (in_range && part == 0) {
-    p.delta[prow] = acc;
-    p.lse2[prow] = real ? p.lse[(bh / p.H) * p.lse_b + (bh % p.H) * p.lse_h + trow] * kLog2e : INFINITY;
+    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in_range && part == 0) {
+      p.delta[prow] = acc;
+      p.lse2[prow] = real ? p.lse[(bh / p.H) * p.lse_b + (bh % p.H) * p.lse_h + trow] * kLog2e : INFINITY;
+    }
   }
 }
 
@@ -255,15 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
                       tma_b);
         }
-        const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + static_cast<size_t>(i) * kBlk;
+        const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + static_cast<size_t>(i) * kBlk;
         bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
         bulk_load(sStats + st * L::kStatBytes + kBlk * 4, p.delta + srow, kBlk * 4, &qdo_full[st]);
         issued = t + 1;
       }
-      if (*abort_flag) {
-        mbar_drain(kv_full, 0);
-        for (int t = (issued > S ? issued - S : 0); t < issued; ++t) mbar_drain(&qdo_full[t % S], (t / S) & 1);
-      }
+      // Every copy issued lands before this thread leaves, whatever the
+      // other roles do (bounded waits; in a normal run they are done).
+      mbar_drain(kv_full, 0);
+      for (int t = (issued > S ? issued - S : 0); t < issued; ++t) mbar_drain(&qdo_full[t % S], (t / S) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -600,8 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
         issued = j + 1;
       }
-      if (*abort_flag)
-        for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
+      for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
     } else if (lane == 1) {
       // the V ring
       tma_prefetch_desc(&tm_v);
@@ -615,8 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
         issued = j + 1;
       }
-      if (*abort_flag)
-        for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&v_full[j % SV], (j / SV) & 1);
+      for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&v_full[j % SV], (j / SV) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -700,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
-    const size_t srow = static_cast<size_t>(bh) * (nblk * kBlk) + qrow;
+    const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + qrow;
     const float lse2 = p.lse2[srow];  // +inf on padding rows: P = 0
     const float dlt = p.delta[srow];
     const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
@@ -838,8 +841,10 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   using L = BwdLayout<D>;
   const long long padded_rows = static_cast<long long>(p.BH) * p.num_blk * kBlk;
   constexpr int kRowsPerBlock = 256 / (D / 8);
+  const long long pre_blocks = (padded_rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  constexpr long long kPreGridMax = 152LL * 8 * 64;  // grid-stride beyond this
   fa_bwd_pre_kernel<D>
-      <<<static_cast<unsigned>((padded_rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(p);
+      <<<static_cast<unsigned>(pre_blocks < kPreGridMax ? pre_blocks : kPreGridMax), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);

@@ -165,10 +165,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           ++c;
         }
       }
-      if (!ok) {
-        // let the copies still in flight land before the CTA exits
-        for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[(j & 1) * S + j % S], group_phase<S>(j) & 1);
-      }
+      // Every copy issued lands before this thread leaves, whatever the
+      // other roles do (bounded waits; in a normal run they are done).
+      for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[(j & 1) * S + j % S], group_phase<S>(j) & 1);
     }
     return;
   }
@@ -545,10 +544,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++c;
         }
       }
-      if (!ok) {
-        for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[j % S], (j / S) & 1);
-        for (int j = (ne > 2 ? ne - 2 : 0); j < ne; ++j) mbar_drain(&q_full[j & 1], (j >> 1) & 1);
-      }
+      // Every copy issued lands before this thread leaves, whatever the
+      // other roles do (bounded waits; in a normal run they are done).
+      for (int j = (c > S ? c - S : 0); j < c; ++j) mbar_drain(&full[j % S], (j / S) & 1);
+      for (int j = (ne > 2 ? ne - 2 : 0); j < ne; ++j) mbar_drain(&q_full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer

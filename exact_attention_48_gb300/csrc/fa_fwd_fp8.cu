@@ -329,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sV + st * L::kKVBytes, &tm_v, &v_full[st], 0, j * kBN, bh_h, bh_b);
         v_issued = j + 1;
       }
-      if (*abort_flag) {
-        mbar_drain(q_full, 0);
-        for (int j = (k_issued > S ? k_issued - S : 0); j < k_issued; ++j) mbar_drain(&k_full[j % S], (j / S) & 1);
-        for (int j = (v_issued > S ? v_issued - S : 0); j < v_issued; ++j) mbar_drain(&v_full[j % S], (j / S) & 1);
-      }
+      // Every copy issued lands before this thread leaves, whatever the
+      // other roles do (bounded waits; in a normal run they are done).
+      mbar_drain(q_full, 0);
+      for (int j = (k_issued > S ? k_issued - S : 0); j < k_issued; ++j) mbar_drain(&k_full[j % S], (j / S) & 1);
+      for (int j = (v_issued > S ? v_issued - S : 0); j < v_issued; ++j) mbar_drain(&v_full[j % S], (j / S) & 1);
     } else if (warp == kWarpMma && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       // S_t = Q_t K_j^T: both K-major, 32 e4m3 (32 bytes) per K step inside

@@ -130,7 +130,10 @@ struct WaitCtl {
   int *status;               // global: [0] = status code, [1] = site of the first timeout
 };
 
-constexpr long long kWaitLimitCycles = 3000000000LL;  // ~1.5 s at 2 GHz
+#ifndef FA_WAIT_LIMIT_CYCLES
+#define FA_WAIT_LIMIT_CYCLES 3000000000LL  // ~1.5 s at 2 GHz (test builds pass a shorter one)
+#endif
+constexpr long long kWaitLimitCycles = FA_WAIT_LIMIT_CYCLES;
 constexpr int kStatusTimeout = 5;                      // FA_ERR_DEVICE_TIMEOUT
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Polls with

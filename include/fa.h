@@ -22,7 +22,11 @@
  *    device pointers owned by the caller, 16-byte aligned, non-null, and
  *    the library keeps none of them after the call returns.
  *  - B, H, N >= 1; d is 64 or 128 (FA_ERR_UNSUPPORTED otherwise);
- *    B*H*N*d < 2^31 elements per tensor.
+ *    B*H*ceil(N/128) < 2^31 (one backward CTA per head and block of 128
+ *    rows must fit a launch grid) and B*H*N*d < 2^39 elements per tensor
+ *    (1 TiB of bf16: TMA byte strides stay below 2^40), which admits every
+ *    tensor a GPU's memory can hold; element offsets are 64-bit
+ *    throughout.
  *  - causal is 0 or 1.  With causal = 1, key j is visible to query i iff
  *    j <= i (square mask, aligned at the top-left).  Fully masked tiles are
  *    skipped.

@@ -75,7 +75,9 @@ def _fwd(lib, *, q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), o=FAKE + (3 << 
     (dict(lse=0), FA_ERR_INVALID_ARGUMENT),
     (dict(k=FAKE + 8), FA_ERR_INVALID_ARGUMENT),          # misaligned
     (dict(o=FAKE + 64), FA_ERR_INVALID_ARGUMENT),         # output overlaps q
-    (dict(B=1 << 14, H=1 << 10, N=1 << 10), FA_ERR_INVALID_ARGUMENT),  # too many elements
+    (dict(B=1 << 14, H=1 << 10, N=1 << 10), FA_ERR_INVALID_ARGUMENT),  # 2^40 elements: beyond TMA's strides
+    (dict(B=1 << 16, H=1 << 16, N=1), FA_ERR_INVALID_ARGUMENT),         # 2^32 heads: beyond a launch grid
+    (dict(B=1 << 15, H=1 << 16, N=1), FA_ERR_INVALID_ARGUMENT),         # 2^31 heads: one past a launch grid
 ])
 def test_fwd_rejects(lib, kw, code):
     assert _fwd(lib, **kw) == code
@@ -97,6 +99,18 @@ def test_bwd_rejects(lib):
     assert _bwd(lib, ws=FAKE + (20 << 30), ws_bytes=need - 1) == FA_ERR_WORKSPACE
     assert _bwd(lib, ws=FAKE + (20 << 30) + 16, ws_bytes=need) == FA_ERR_INVALID_ARGUMENT  # not 256-aligned
     assert _bwd(lib, ws=FAKE + (3 << 30), ws_bytes=need) == FA_ERR_INVALID_ARGUMENT        # overlaps o
+
+
+def test_sizes_beyond_2_31_elements_are_accepted(lib):
+    """Tensors of 2^31 elements and more pass the host checks (element
+    offsets are 64-bit): the workspace query answers for them.  2^21 heads
+    of 1032 rows at d = 128 are 2.8e11 elements per tensor."""
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for B, H, N, d in [(1 << 11, 1 << 10, 1032, 128), (1, 1, (1 << 24) + 3, 128), (1 << 16, 1 << 8, 128, 64)]:
+        assert B * H * N * d >= 1 << 31
+        Np = (N + 127) // 128 * 128
+        assert lib.fa_bwd_workspace_bytes(B, H, N, d) == 2 * r256(B * H * Np * 4)
+    assert lib.fa_bwd_workspace_bytes(1 << 16, 1 << 16, 1, 64) == 0     # 2^32 heads: rejected
 
 
 def test_workspace_bytes(lib):

@@ -95,15 +95,59 @@ def test_long_context_b1h16n16384d128():
     _run(LONG_B1H16N16384D128, heads_max=2, full_torch=False)
 
 
-@pytest.mark.parametrize("N", [512, 2048, 8192, 16384])
+@pytest.mark.parametrize("N", [512, 1024, 2048, 8192, 16384])
 @pytest.mark.parametrize("causal", [False, True])
 def test_sweep_points_d128(N, causal):
     _run(sweep(N, 128, causal), heads_max=2, full_torch=(N <= 8192))
 
 
-@pytest.mark.parametrize("N", [512, 4096])
-def test_sweep_points_d64(N):
-    _run(sweep(N, 64, True), heads_max=2)
+@pytest.mark.parametrize("N,causal", [(512, True), (1024, False), (2048, False), (4096, True), (16384, False),
+                                      (16384, True)])
+def test_sweep_points_d64(N, causal):
+    _run(sweep(N, 64, causal), heads_max=2, full_torch=(N <= 8192))
+
+
+def _torch_ref_grads(q, k, v, do, causal, scale, heads_per_batch=8):
+    """dQ, dK, dV of PyTorch fp32 attention on the GPU (autograd through
+    the materialised softmax), a few heads at a time, from the same bf16
+    inputs upcast."""
+    B, H, N, d = q.shape
+    qf, kf, vf, dof = (t.reshape(B * H, N, d) for t in (q, k, v, do))
+    outs = [torch.empty(B * H, N, d, device=q.device, dtype=torch.float32) for _ in range(3)]
+    mask = torch.ones(N, N, device=q.device, dtype=torch.bool).triu(1) if causal else None
+    for h0 in range(0, B * H, heads_per_batch):
+        sl = slice(h0, min(B * H, h0 + heads_per_batch))
+        a, b, c = (t[sl].float().requires_grad_(True) for t in (qf, kf, vf))
+        s = (a @ b.transpose(1, 2)) * scale
+        if causal:
+            s = s.masked_fill(mask, float("-inf"))
+        o = torch.softmax(s, -1) @ c
+        ga, gb, gc = torch.autograd.grad(o, (a, b, c), dof[sl].float())
+        for dst, g in zip(outs, (ga, gb, gc)):
+            dst[sl] = g
+        del a, b, c, s, o, ga, gb, gc
+    return [t.view(B, H, N, d) for t in outs]
+
+
+@pytest.mark.parametrize("N,d,causal", [(2048, 128, False), (4096, 128, True), (2048, 64, False)])
+def test_sweep_point_gradients_every_head(N, d, causal):
+    """Every head's dQ, dK, dV of a sweep point against PyTorch fp32
+    attention on the GPU (the per-head bound: 2e-2 x max|grad| of the
+    reference), beside the oracle's sampled heads."""
+    w = sweep(N, d, causal)
+    q, k, v, do = draw(w, device="cuda")
+    o, lse = fa_fwd(q, k, v, w.causal, w.scale)
+    grads = fa_bwd(q, k, v, o, do, lse, w.causal, w.scale)
+    assert fa_device_status() == 0
+    refs = _torch_ref_grads(q, k, v, do, w.causal, w.scale)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+        g, r = g.float().reshape(w.B * w.H, -1), r.reshape(w.B * w.H, -1)
+        assert bool(torch.isfinite(g).all()), name
+        err = (g - r).abs().amax(dim=1)
+        bound = 2e-2 * r.abs().amax(dim=1) + 1e-6
+        worst = int(torch.argmax(err / bound))
+        assert bool((err <= bound).all()), (f"{w.name} {name}: head {worst} err {float(err[worst]):.3e} "
+                                            f"> {float(bound[worst]):.3e}")
 
 
 def _bench_problem(w):

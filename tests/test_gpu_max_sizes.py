@@ -1,6 +1,7 @@
-"""Large-extent cases: many heads (a grid of tens of thousands of CTAs) and
-a key/value cache of a million keys with a ragged last tile for decode,
-each checked on sampled rows against the oracle."""
+"""Large-extent cases: many heads (a grid of tens of thousands of CTAs),
+tensors of more than 2^31 elements, and a key/value cache of a million keys
+with a ragged last tile for decode, each checked on sampled rows against
+the oracle."""
 import math
 
 import numpy as np
@@ -31,6 +32,33 @@ def test_many_heads_short_sequences():
         refs = oracle.bwd(q[b, h], k[b, h], v[b, h], do[b, h], True, scale)
         for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
             check_grad(g, r, name, f"head ({b},{h})")
+
+
+def test_tensors_beyond_2_31_elements():
+    """B*H = 16384 heads of N = 1032 rows at d = 128: 2.16e9 elements per
+    tensor (4.3 GB of bf16, more than 2^31 elements), forward and backward.
+    The heads checked against the oracle include the first, the one that
+    straddles element 2^31, the first one wholly past it and the last; all
+    outputs are finite."""
+    B, H, N, d = 64, 256, 1032, 128
+    assert B * H * N * d > 1 << 31
+    scale = 1 / math.sqrt(d)
+    q, k, v, do = draw_shape(B, H, N, d, 93, 1.0, "cuda", torch.bfloat16)
+    o, lse = fa_fwd(q, k, v, False)
+    dq, dk, dv = fa_bwd(q, k, v, o, do, lse, False)
+    assert fa_device_status() == 0
+    straddle = (1 << 31) // (N * d)           # head whose elements cross index 2^31
+    assert straddle * N * d < 1 << 31 < (straddle + 1) * N * d
+    for hh in (0, straddle, straddle + 1, B * H - 1):
+        b, h = divmod(hh, H)
+        o_ref, lse_ref = oracle.fwd(q[b, h], k[b, h], v[b, h], False, scale)
+        check_o(o[b, h], o_ref, f"head {hh}")
+        check_lse(lse[b, h], lse_ref, f"head {hh}")
+        refs = oracle.bwd(q[b, h], k[b, h], v[b, h], do[b, h], False, scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            check_grad(g, r, name, f"head {hh}")
+    for t in (o, lse, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
 
 
 def test_decode_million_keys():
