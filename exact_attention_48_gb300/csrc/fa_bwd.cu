@@ -45,6 +45,20 @@ constexpr uint32_t kTmemCols = 512;
 // sub-partition runs two row warps and one can issue while the other waits.
 constexpr int kThreads = 384;
 constexpr int kRowWarps = 8;  // row warps; each signals its barriers once (lane 0)
+// The dK/dV kernel splits each key row over RG row warpgroups (RG = 2 or
+// 4, a template parameter): RG = 4 gives each warp a quarter of the 128
+// query columns, twice the warps per SM sub-partition to hide the latency
+// of the row phases and half the work per thread (+3 % on long non-causal
+// heads, measured); with few query blocks per CTA (causal) the larger CTA
+// costs more than it hides (-8 % causal N = 4096), so causal keeps RG = 2.
+// Per element the arithmetic is the same either way: the results are
+// bitwise equal.
+template <int RG>
+struct KvRows {
+  static constexpr int kThreads = 128 + 128 * RG;
+  static constexpr int kRowWarps = 4 * RG;
+  static constexpr int kCols = kBlk / RG;  // query columns per row thread
+};
 
 // ------------------------------------------------------------------ pre
 
@@ -152,14 +166,15 @@ struct BwdLayout {
 // so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
 // dV(t+1) and S^T(t+2) run.  Each product that overwrites a TMEM region
 // comes after the one that reads it (the tensor core runs them in order).
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, bool VARLEN, int RG>
+__global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
   using L = BwdLayout<D>;
   constexpr int S = L::kStages;
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  constexpr int kKvCols = KvRows<RG>::kCols;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -212,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, kRowWarps);
-    mbar_init(ds_ready, kRowWarps);
+    mbar_init(p_ready, KvRows<RG>::kRowWarps);
+    mbar_init(ds_ready, KvRows<RG>::kRowWarps);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -317,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint64_t bdo = do_mn(t);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)  // P^T of queries [64h, 64h+64) sits at columns 64h..
-            mma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bdo, mnmajor_step(kk)), kIdescKV,
-                   (t > 0 || kk > 0));
+          for (int kk = 0; kk < kBlk / 16; ++kk)  // P^T of queries [c g, c g + c) sits at columns c g.. (c = kKvCols)
+            mma_ts(tDV, tS + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8, desc_add(bdo, mnmajor_step(kk)),
+                   kIdescKV, (t > 0 || kk > 0));
         }
         // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
         // first, reads P^T(t) before S^T(t+1) overwrites it
@@ -335,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint64_t bq = q_mn(t);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS^T of queries [64h, 64h+64) sits at columns 128 + 64h..
-            mma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bq, mnmajor_step(kk)), kIdescKV,
-                   (t > 0 || kk > 0));
+          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS^T of queries [c g, c g + c) sits at columns 128 + c g..
+            mma_ts(tDK, tDP + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8, desc_add(bq, mnmajor_step(kk)),
+                   kIdescKV, (t > 0 || kk > 0));
         }
         tc_commit(&qdo_empty[st]);
         if (more) issue_dp(t + 1);
@@ -348,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ key rows
-    const int half = (warp >> 2) - 1;  // query columns [64 half, 64 half + 64)
+    const int grp = (warp >> 2) - 1;  // query columns [kKvCols grp, kKvCols (grp + 1))
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the block
     const int key = jblk * kBlk + r;
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
     const bool key_ok = key < N;
-    const int c0 = half * 64;  // first query column of this half
+    const int c0 = grp * kKvCols;  // first query column of this quarter
     bool ok = true;
 
     for (int t = 0; t < n_q; ++t) {
@@ -368,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 *del4 = reinterpret_cast<const float4 *>(stats + kBlk + c0);
       const bool diag = CAUSAL && (i == jblk);
 
-      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + 32).
+      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + kKvCols / 2).
       // (The stage's copies are complete once S^T(t) is; the rows wait on
       // them too so that the statistics' copy is visible to their loads.
       // The stage cannot be refilled before ds_ready(t).)
@@ -379,92 +394,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // P^T of this half row in fp32 pairs (kept for phase 2) and as bf16
+      // P^T of this quarter row in fp32 pairs (kept for phase 2) and as bf16
       // pairs in TMEM.  Key rows past N (zero rows of K, so S = 0) get a
       // finite P that only reaches their own dV, dK rows, which are not
       // stored: no mask needed.
-      float2 pf[32];
-      uint32_t sva[2][32];
+      constexpr int kCh = kKvCols / 32;  // 32-column chunks per row thread
+      float2 pf[kKvCols / 2];
+      {
+        uint32_t sva[kCh][32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
+        for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
+        for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(sva[ch]);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const uint32_t(&sv)[32] = sva[ch];
-        uint32_t pk[16];
+        for (int ch = 0; ch < kCh; ++ch) {
+          const uint32_t(&sv)[32] = sva[ch];
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int qh = ch * 32 + e;  // query column within the half
-          const float4 l4 = lse4[qh / 4];
-          const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), make_float2(c, c),
-                                   make_float2(-l4.x, -l4.y));
-          const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
-                                   make_float2(c, c), make_float2(-l4.z, -l4.w));
-          float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
-          if (diag) {
+          for (int e = 0; e < 32; e += 4) {
+            const int qh = ch * 32 + e;  // query column within this thread's columns
+            const float4 l4 = lse4[qh / 4];
+            const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                     make_float2(c, c), make_float2(-l4.x, -l4.y));
+            const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                     make_float2(c, c), make_float2(-l4.z, -l4.w));
+            float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+            if (diag) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
+              for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
+            }
+            pf[qh / 2] = make_float2(pr[0], pr[1]);
+            pf[qh / 2 + 1] = make_float2(pr[2], pr[3]);
+            pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
+            pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
           }
-          pf[qh / 2] = make_float2(pr[0], pr[1]);
-          pf[qh / 2 + 1] = make_float2(pr[2], pr[3]);
-          pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
-          pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+          tmem_st16(tS + c0 + ch * 16, pk);  // over scores of this thread's columns, already read
         }
-        tmem_st16(tS + c0 + ch * 16, pk);  // over scores of this half, already read
       }
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(p_ready);
 
-      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 pairs over this half's own,
-      // already read, dP^T columns.
+      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 pairs over this quarter's
+      // own, already read, dP^T columns.
       ok = mbar_wait(dp_full, t & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t dpa[2][32];
+      {
+        uint32_t dpa[kCh][32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
+        for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(dpa[ch]);
+        for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(dpa[ch]);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const uint32_t(&dpv)[32] = dpa[ch];
-        uint32_t dk[16];
+        for (int ch = 0; ch < kCh; ++ch) {
+          const uint32_t(&dpv)[32] = dpa[ch];
+          uint32_t dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int qh = ch * 32 + e;
-          const float4 d4 = del4[qh / 4];
-          const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
-                                   make_float2(-d4.x, -d4.y));
-          const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
-                                   make_float2(-d4.z, -d4.w));
-          const float2 ds01 = fmul2(pf[qh / 2], g01);
-          const float2 ds23 = fmul2(pf[qh / 2 + 1], g23);
-          dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
-          dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
+          for (int e = 0; e < 32; e += 4) {
+            const int qh = ch * 32 + e;
+            const float4 d4 = del4[qh / 4];
+            const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                     make_float2(-d4.x, -d4.y));
+            const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                     make_float2(-d4.z, -d4.w));
+            const float2 ds01 = fmul2(pf[qh / 2], g01);
+            const float2 ds23 = fmul2(pf[qh / 2 + 1], g23);
+            dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
+            dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
+          }
+          tmem_st16(tDP + c0 + ch * 16, dk);
         }
-        tmem_st16(tDP + c0 + ch * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(ds_ready);
     }
-    // epilogues: the first half writes dV, the second dK (scale applied here)
+    // epilogues: the first half of the row groups writes dV, the second dK
+    // (scale applied here), each group a D / (RG / 2) column slice
     if (ok) {
       ok = mbar_wait(acc_done, 0, ctl, kSiteMmaDone);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      if (half == 0)
-        store_acc_row<D>(tmem + kColDV + lane_base, p.dv + row_offset(p.sdv, bh, p.H, row0 + key), key_ok, 1.0f);
+      constexpr int kW = D / (RG / 2);  // columns per group
+      const int col = (grp % (RG / 2)) * kW;
+      if (grp < RG / 2)
+        store_acc_row<kW>(tmem + kColDV + lane_base + col, p.dv + row_offset(p.sdv, bh, p.H, row0 + key) + col,
+                          key_ok, 1.0f);
       else
-        store_acc_row<D>(tmem + kColDK + lane_base, p.dk + row_offset(p.sdk, bh, p.H, row0 + key), key_ok,
-                         p.scale);
+        store_acc_row<kW>(tmem + kColDK + lane_base + col, p.dk + row_offset(p.sdk, bh, p.H, row0 + key) + col,
+                          key_ok, p.scale);
     }
   }
 
@@ -827,11 +851,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename Kern>
-cudaError_t launch_main(Kern kern, unsigned grid, uint32_t smem, const CUtensorMap &tq, const CUtensorMap &tk,
-                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream) {
+cudaError_t launch_main(Kern kern, unsigned grid, int threads, uint32_t smem, const CUtensorMap &tq,
+                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
+                        cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, threads, smem, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
@@ -849,10 +874,14 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN>, grid, L::kSmemRequest, tq, tk, tv, tdo, p, stream);
+  // (long non-causal heads: four row groups; causal: two, see KvRows)
+  constexpr int RG = CAUSAL ? 2 : 4;
+  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG>, grid, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk, tv,
+                  tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo, p, stream);
+  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
+                  p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
   return cudaSuccess;
