@@ -58,12 +58,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 # Test builds: the same sources with extra preprocessor definitions, linked
 # into their own folder under _build/ (never into libfa.so).  The one used
-# by the tests shortens every pipeline wait to FA_WAIT_LIMIT_CYCLES and
+# by the tests shortens every pipeline wait to FA_WAIT_LIMIT_NS (1 ms) and
 # leaves out the forward's first V load, so that the bounded-wait path
 # (FA_ERR_DEVICE_TIMEOUT through fa_device_status) can be exercised
 # without any kernel waiting for long.
 VARIANTS = {
-    "stalltest": ["-DFA_WAIT_LIMIT_CYCLES=2000000LL", "-DFA_TEST_SKIP_FIRST_V_LOAD"],
+    "stalltest": ["-DFA_WAIT_LIMIT_NS=1000000ULL", "-DFA_TEST_SKIP_FIRST_V_LOAD"],
 }
 
 

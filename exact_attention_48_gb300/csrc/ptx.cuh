@@ -130,28 +130,31 @@ struct WaitCtl {
   int *status;               // global: [0] = status code, [1] = site of the first timeout
 };
 
-#ifndef FA_WAIT_LIMIT_CYCLES
-#define FA_WAIT_LIMIT_CYCLES 3000000000LL  // ~1.5 s at 2 GHz (test builds pass a shorter one)
+#ifndef FA_WAIT_LIMIT_NS
+#define FA_WAIT_LIMIT_NS 1500000000ULL  // 1.5 s (test builds pass a shorter one)
 #endif
-constexpr long long kWaitLimitCycles = FA_WAIT_LIMIT_CYCLES;
+constexpr uint64_t kWaitLimitNs = FA_WAIT_LIMIT_NS;
 constexpr int kStatusTimeout = 5;                      // FA_ERR_DEVICE_TIMEOUT
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Polls with
 // try_wait (which suspends the thread until the phase completes or a short
 // hardware limit passes); every 256 polls it checks whether another role of
-// the CTA has given up and whether kWaitLimitCycles SM cycles have passed.
-// Returns false on either (and records the first timeout in the status
-// word).  The SM cycle counter is used rather than the global timer because
-// it is cheap to read.
+// the CTA has given up and whether kWaitLimitNs have passed on the GPU's
+// global nanosecond timer.  Returns false on either (and records the first
+// timeout in the status word).  The global timer, unlike an SM's cycle
+// counter, means the same on every SM and keeps wall-clock time whatever
+// the SM clock, so a CTA resumed on another SM after a preemption measures
+// its wait correctly; time the CTA spends off the GPU (a context switch to
+// another process) counts too, which a 1.5 s limit leaves ample room for.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &ctl, int site) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
+  const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*ctl.abort_flag) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
         *ctl.abort_flag = 1;
         if (atomicCAS(ctl.status, 0, kStatusTimeout) == 0) atomicExch(ctl.status + 1, site);
         return false;
@@ -175,11 +178,11 @@ __device__ __forceinline__ float2 add_bf16x2_f32(float2 acc, uint32_t b) {
 // Same, without consulting the abort flag: used on the way out to drain
 // asynchronous copies and MMAs that are still in flight.
 __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
-  const long long t0 = clock64();
+  const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 255u && clock64() - t0 > kWaitLimitCycles) return false;
+    if ((n & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

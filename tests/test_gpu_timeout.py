@@ -4,7 +4,7 @@ usable.
 
 The failure is made without faulting or hanging anything: a test build of
 the library (build.py's "stalltest" variant, its own .so under _build/)
-shortens every wait to 2e6 SM cycles (about a millisecond) and leaves out
+shortens every wait to a millisecond and leaves out
 the forward's first V load, so the MMA thread's wait for it runs out.  The
 kernel then raises its abort flag, drains the copies and products it
 issued, frees its TMEM and exits; fa_device_status reports the timeout
