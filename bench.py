@@ -510,14 +510,16 @@ def run_ours(args):
 
     bwd_on = w.backward  # the forward-only workload times the forward alone
 
-    def step(evs=None):
+    def step(evs=None, kernel_times=False):
         if evs is not None:
             evs[0].record(stream)
         pb.fwd(q, k, v, o, lse)
         if evs is not None:
             evs[1].record(stream)
         if bwd_on:
-            if evs is not None:
+            if kernel_times:
+                # events between the backward's kernels; the library then runs
+                # them one after the other instead of side by side
                 fa_debug_time_next_bwd(evs[2], evs[3], evs[4])
             pb.bwd(q, k, v, o, do, lse, dq, dk, dv)
         if evs is not None:
@@ -555,6 +557,17 @@ def run_ours(args):
     clk = clocks.stop(t_wall0, t_wall1)
     if fa_device_status() != 0:
         raise SystemExit("device status error in the timed region")
+    # Per-kernel durations for the roofline: a second timed pass with events
+    # between the backward's kernels (which makes them run one after the
+    # other; the main timed region above runs the dQ kernel next to the
+    # dK/dV kernel).
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(min(args.steps, 50))]
+    if bwd_on:
+        for i in range(len(kevs)):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            step(kevs[i], kernel_times=True)
+        torch.cuda.synchronize()
 
     flops_step = w.flops_fwd() + (w.flops_bwd() if bwd_on else 0.0)
     total_ms = start.elapsed_time(stop)
@@ -564,8 +577,8 @@ def run_ours(args):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     if bwd_on:
         bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
-        dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-        dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+        dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in kevs)
+        dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in kevs)
 
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
@@ -616,6 +629,9 @@ def run_ours(args):
                      "peak_source": (f"{peak_src} {peak_kind}"
                                      + (", x2 for the fp8 path (nominal fp8/bf16 ratio)" if w.layout == "fp8" else "")),
                      "flops_per_launch": dom_flops, "traffic": traffic},
+        "kernel_timing": ("per-kernel durations from a second timed pass of the same steps with events between "
+                          "the backward's kernels (which then run one after the other; in the main timed region "
+                          "the dQ kernel runs next to the dK/dV kernel on a side stream)") if bwd_on else None,
         "gpu_launches": (4 if bwd_on else 1) * args.steps,  # fwd; bwd pre, dK/dV, dQ
         "clocks": clk,
     }

@@ -283,7 +283,7 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
                      const Strides &sv, const void *o, const Strides &so, const void *dO, const Strides &sdo,
                      const float *lse, void *dq, const Strides &sdq, void *dk, const Strides &sdk, void *dv,
                      const Strides &sdv, const RowAxis &ax, int H, int d, int causal, float scale, void *workspace,
-                     size_t workspace_bytes, cudaStream_t stream) {
+                     size_t workspace_bytes, cudaStream_t stream, bool concurrent = true) {
   const int B = ax.B, N = ax.N, SB = ax.slots(), R = ax.rows();
   fa_status_t st = check_common(B, H, N, d, causal, scale);
   if (st == FA_OK && ax.cu) st = check_common(1, H, R, d, causal, scale);
@@ -371,7 +371,8 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   fa_status_t rc = FA_OK;
   const cudaEvent_t ev[3] = {t_bwd_ev[0], t_bwd_ev[1], t_bwd_ev[2]};
   t_bwd_ev[0] = t_bwd_ev[1] = t_bwd_ev[2] = nullptr;
-  if (!p.status || launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream, ev[0] ? ev : nullptr) != cudaSuccess)
+  if (!p.status ||
+      launch_bwd(d, causal != 0, tq, tk, tv, tdo, p, stream, ev[0] ? ev : nullptr, concurrent) != cudaSuccess)
     rc = FA_ERR_CUDA;
   if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) rc = FA_ERR_CUDA;
   return rc;
@@ -617,6 +618,15 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
   const Strides s = contiguous(H, N, d);
   return bwd_impl(q, s, k, s, v, s, o, s, dO, s, lse, dq, s, dk, s, dv, s, RowAxis{B, N, nullptr, 0}, H, d, causal,
                   scale, workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_sequential(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                              int causal, float scale, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  const Strides s = contiguous(H, N, d);
+  return bwd_impl(q, s, k, s, v, s, o, s, dO, s, lse, dq, s, dk, s, dv, s, RowAxis{B, N, nullptr, 0}, H, d, causal,
+                  scale, workspace, workspace_bytes, stream, false);
 }
 
 fa_status_t fa_bwd_strided(const void *q, const int64_t *q_strides, const void *k, const int64_t *k_strides,

@@ -860,9 +860,34 @@ cudaError_t launch_main(Kern kern, unsigned grid, int threads, uint32_t smem, co
   return cudaGetLastError();
 }
 
+// A side stream and two events per host thread and device, for running the
+// dQ kernel next to the dK/dV kernel (created on first use, kept until the
+// process ends).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t side_stream(SideStream **out) {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream res[kMaxDevices];
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream &r = res[dev];
+  if (!r.stream) {
+    if ((e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&r.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  }
+  *out = &r;
+  return cudaSuccess;
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
-                         const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
+                         const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev, bool concurrent) {
   using L = BwdLayout<D>;
   const long long padded_rows = static_cast<long long>(p.BH) * p.num_blk * kBlk;
   constexpr int kRowsPerBlock = 256 / (D / 8);
@@ -873,9 +898,28 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);
-  if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
   // (long non-causal heads: four row groups; causal: two, see KvRows)
   constexpr int RG = CAUSAL ? 2 : 4;
+  if (concurrent && !ev) {
+    // The dQ kernel reads only the inputs and the pre-kernel's statistics,
+    // so it runs on a side stream next to the dK/dV kernel: each grid is
+    // 13.5 waves of one CTA per SM at the bench shape, and the two
+    // together leave fewer SMs idle in a last wave than one after the
+    // other.  The caller's stream waits for both before anything after.
+    SideStream *side = nullptr;
+    if ((e = side_stream(&side)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(side->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
+    e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG>, grid, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk,
+                    tv, tdo, p, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
+                    p, side->stream);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(stream, side->join, 0);
+  }
+  if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
   e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG>, grid, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk, tv,
                   tdo, p, stream);
   if (e != cudaSuccess) return e;
@@ -890,22 +934,23 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev) {
+                       const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream, const cudaEvent_t *ev,
+                       bool concurrent) {
   // (the packed-sequence mode is a template parameter: the batched kernels
   // carry none of its per-block work)
   const bool v = p.cu_seqlens != nullptr;
   if (d == 64) {
     if (causal)
-      return v ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, stream, ev)
-               : launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, stream, ev);
-    return v ? launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, stream, ev)
-             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, stream, ev);
+      return v ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, stream, ev, concurrent)
+               : launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, stream, ev, concurrent);
+    return v ? launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, stream, ev, concurrent)
+             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, stream, ev, concurrent);
   }
   if (causal)
-    return v ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, stream, ev)
-             : launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, stream, ev);
-  return v ? launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, stream, ev)
-           : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, stream, ev);
+    return v ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, stream, ev, concurrent)
+             : launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, stream, ev, concurrent);
+  return v ? launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, stream, ev, concurrent)
+           : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, stream, ev, concurrent);
 }
 
 }  // namespace fa

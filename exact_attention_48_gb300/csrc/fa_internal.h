@@ -7,6 +7,8 @@
 #include <cuda_runtime_api.h>
 #include <cstdint>
 
+#include "../../include/fa.h"
+
 namespace fa {
 
 // Where a kernel gave up waiting (second word of the device status block).
@@ -146,9 +148,24 @@ cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensor
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 
 // ev[0..2] (all null or all set) are recorded before the dK/dV kernel,
-// between it and the dQ kernel, and after the dQ kernel.
+// between it and the dQ kernel, and after the dQ kernel; the two kernels
+// then run one after the other.  Without events and with `concurrent`, the
+// dQ kernel runs on a side stream next to the dK/dV kernel, joined before
+// the call returns.
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
-                       cudaStream_t stream, const cudaEvent_t *ev);
+                       cudaStream_t stream, const cudaEvent_t *ev, bool concurrent);
+
+}  // namespace fa
+
+// The backward pass of fa_bwd with its two main kernels one after the
+// other on `stream` (no side stream): used by fa_bwd_noalloc.  Internal
+// (hidden visibility: not exported from libfa.so).
+extern "C" fa_status_t fa_bwd_sequential(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                              int causal, float scale, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+namespace fa {
 
 }  // namespace fa

@@ -8,6 +8,8 @@
 // cudaMalloc nor let it take one with cudaMallocAsync.  fa_bwd_noalloc
 // gives them the same backward pass with its scratch (the per-row D and
 // logsumexp arrays) in a fixed array of this library's own device memory.
+// Its two main kernels run one after the other on the caller's stream (no
+// side stream is created for it).
 //
 // The array is a file-scope __device__ variable of FA_NOALLOC_SCRATCH_BYTES
 // bytes: every GPU that loads the library holds it until the process
@@ -29,6 +31,7 @@
 #include <cstdint>
 
 #include "../../include/fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -62,6 +65,6 @@ extern "C" fa_status_t fa_bwd_noalloc(const void *q, const void *k, const void *
   void *scratch = nullptr;
   const fa_status_t st = scratch_address(&scratch);
   if (st != FA_OK) return st;
-  return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, causal, scale, scratch, FA_NOALLOC_SCRATCH_BYTES,
-                stream);
+  return fa_bwd_sequential(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, causal, scale, scratch,
+                           FA_NOALLOC_SCRATCH_BYTES, stream);
 }

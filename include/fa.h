@@ -20,7 +20,10 @@
  *    whose d elements are contiguous.  lse is fp32, contiguous [B, H, N].
  *    All pointers are
  *    device pointers owned by the caller, 16-byte aligned, non-null, and
- *    the library keeps none of them after the call returns.
+ *    the library keeps none of them after the call returns.  The library
+ *    owns only a device status word per device, and for fa_bwd and its
+ *    strided and packed forms one side stream and two events per host
+ *    thread and device.
  *  - B, H, N >= 1; d is 64 or 128 (FA_ERR_UNSUPPORTED otherwise);
  *    B*H*ceil(N/128) < 2^31 (one backward CTA per head and block of 128
  *    rows must fit a launch grid) and B*H*N*d < 2^39 elements per tensor
@@ -103,6 +106,11 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                    bytes, 256-byte aligned, or NULL to let the library
  *                    take it with cudaMallocAsync/cudaFreeAsync on `stream`.
  * No atomics are used: dq, dk and dv are bitwise reproducible run to run.
+ * The dK/dV kernel runs on `stream` and the dQ kernel next to it on a side
+ * stream of the library's (one per host thread and device, created on the
+ * first call with two events, kept until the process exits); `stream`
+ * waits for both before any work enqueued after the call, so the ordering
+ * a caller sees is that of a single stream.
  */
 FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
                    const void *dO, const float *lse, void *dq, void *dk, void *dv,
@@ -267,7 +275,8 @@ FA_API fa_status_t fa_fwd_decode(const void *q, const int64_t *q_strides, const 
  * Backward pass for callers that must not allocate device memory: the same
  * computation, arguments, layouts and results as fa_bwd, but with no
  * workspace argument and no allocation of any kind (no cudaMalloc,
- * cudaMallocAsync or cudaFree).  Its scratch lives in a fixed array of the
+ * cudaMallocAsync or cudaFree, and no side stream: its kernels run one
+ * after the other on `stream`).  Its scratch lives in a fixed array of the
  * library (FA_NOALLOC_SCRATCH_BYTES); calls that would need more return
  * FA_ERR_WORKSPACE without launching anything.
  *
@@ -311,7 +320,8 @@ FA_API int fa_debug_last_wait_site(void);
  * records, on its stream, `start` right before the launch of its dK/dV
  * kernel, `mid` between that kernel and its dQ kernel, and `stop` right
  * after the dQ kernel, so both kernels can be timed with
- * cudaEventElapsedTime.  The events are created and owned by the caller;
+ * cudaEventElapsedTime (that call runs the two kernels one after the
+ * other on its stream, not side by side).  The events are created and owned by the caller;
  * the hook is used once and then cleared.  Returns FA_ERR_INVALID_ARGUMENT
  * if any event is NULL.
  */
