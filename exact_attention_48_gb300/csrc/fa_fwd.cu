@@ -95,7 +95,7 @@ struct SoftmaxArgs {
 };
 
 // Online softmax of one 128-row tile: one query row per thread.
-template <int D, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdParams &p, const WaitCtl &ctl, int bh,
                                              int warp, int lane) {
   const int wq = warp & 3;
@@ -110,12 +110,17 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
   float m_run = -INFINITY, l_run = 0.0f, lb_run = 0.0f;
   bool ok = true;
 
-  for (int j = 0; j < a.n_kv; ++j) {
-    ok = mbar_wait(a.s_full, j & 1, ctl, kSiteSFull);
-    if (!__all_sync(0xffffffffu, ok)) {
-      ok = false;
-      break;
-    }
+  // One key block.  `mask` (a run-time flag, or a compile-time one) says
+  // whether the block needs the causal or ragged-end mask, which only a
+  // tile's last block can.  With the flag known at compile time, two copies
+  // of the body keep the masking instructions out of every other block.
+  // Measured: the causal kernels with one body and a run-time test ran
+  // their ALU pipe at 41 % against 23 % without a mask, and the two copies
+  // made them 8-18 % faster (and the d = 64 kernels 5 %); only the
+  // batched non-causal d = 128 kernel was 2 % faster with the one body.
+  auto block = [&](const int j, auto mask) -> bool {
+    const bool MASK = mask;
+    if (!__all_sync(0xffffffffu, mbar_wait(a.s_full, j & 1, ctl, kSiteSFull))) return false;
     tc_fence_after();
     uint32_t s[4][32];
 #pragma unroll
@@ -124,9 +129,8 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(s[q4]);
 
     // Masking: causal diagonal block and the ragged last key block.
-    const bool need_mask = (j == a.diag) || ((j + 1) * kBN > N);
     int lim = kBN - 1;  // last visible column of this row
-    if (need_mask) {
+    if (MASK) {
       lim = min(lim, N - 1 - j * kBN);
       if (j == a.diag) lim = min(lim, row);
       const uint32_t hide = __float_as_uint(neg ? INFINITY : -INFINITY);
@@ -184,7 +188,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
       for (int i = 0; i < 32; i += 2) {
         const float2 x = ffma2(make_float2(__uint_as_float(s[q4][i]), __uint_as_float(s[q4][i + 1])), cc, nm);
         float p0 = ex2(x.x), p1 = ex2(x.y);
-        if (need_mask) {
+        if (MASK) {
           p0 = (q4 * 32 + i <= lim) ? p0 : 0.0f;
           p1 = (q4 * 32 + i + 1 <= lim) ? p1 : 0.0f;
         }
@@ -201,11 +205,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     // complete; the wait only makes that explicit).  Rows that keep their
     // max leave O alone, and the next product simply accumulates into it.
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      ok = mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone))) return false;
       {
         tc_fence_after();
 #pragma unroll 1
@@ -237,6 +237,20 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
         sb = fadd2(sb, sbq);
       }
       lb_run = lb_run * alpha + (sb.x + sb.y);
+    }
+    return true;
+  };
+  constexpr bool kTwoBodies = !(D == 128 && !CAUSAL && !VARLEN);
+  for (int j = 0; j < a.n_kv; ++j) {
+    const bool need_mask = (j == a.diag) || ((j + 1) * kBN > N);
+    bool cont;
+    if constexpr (kTwoBodies)
+      cont = need_mask ? block(j, MaskTag<true>{}) : block(j, MaskTag<false>{});
+    else
+      cont = block(j, need_mask);
+    if (!cont) {
+      ok = false;
+      break;
     }
   }
 
@@ -489,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     a.grow0 = qb * 2 * kBM + t * kBM;
     a.N = N;
     a.row0 = row0;
-    softmax_tile<D, VARLEN>(a, p, ctl, bh, warp, lane);
+    softmax_tile<D, CAUSAL, VARLEN>(a, p, ctl, bh, warp, lane);
   }
 
   tc_fence_before();

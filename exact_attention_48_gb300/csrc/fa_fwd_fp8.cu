@@ -83,12 +83,13 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
   float m_run = -INFINITY, l_run = 0.0f, lb_run = 0.0f;
   bool ok = true;
 
-  for (int j = 0; j < a.n_kv; ++j) {
-    ok = mbar_wait(a.s_full, j & 1, ctl, kSiteSFull);
-    if (!__all_sync(0xffffffffu, ok)) {
-      ok = false;
-      break;
-    }
+  // One key block; MASK: the causal or ragged-end mask, which only a
+  // tile's last block needs.  Two copies of the body (MaskTag) keep the
+  // masking instructions out of every other block (measured: 5 % faster
+  // than one body with a run-time test, non-causal).
+  auto block = [&](const int j, auto mask_tag) -> bool {
+    const bool MASK = mask_tag;
+    if (!__all_sync(0xffffffffu, mbar_wait(a.s_full, j & 1, ctl, kSiteSFull))) return false;
     tc_fence_after();
     uint32_t s[4][32];
 #pragma unroll
@@ -96,9 +97,8 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(s[q4]);
 
-    const bool need_mask = (CAUSAL && j == a.diag) || ((j + 1) * kBN > N);
     int lim = kBN - 1;
-    if (need_mask) {
+    if (MASK) {
       lim = min(lim, N - 1 - j * kBN);
       if (CAUSAL && j == a.diag) lim = min(lim, row);
       const uint32_t hide = __float_as_uint(neg ? INFINITY : -INFINITY);
@@ -158,7 +158,7 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
         const float2 x23 =
             ffma2(make_float2(__uint_as_float(s[q4][i + 2]), __uint_as_float(s[q4][i + 3])), cc, bias);
         float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
-        if (need_mask) {
+        if (MASK) {
           const int k0 = q4 * 32 + i;
           p0 = (k0 <= lim) ? p0 : 0.0f;
           p1 = (k0 + 1 <= lim) ? p1 : 0.0f;
@@ -174,11 +174,7 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
     tmem_st_wait();
 
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      ok = mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone))) return false;
       tc_fence_after();
 #pragma unroll 1
       for (int ch = 0; ch < kD / 16; ++ch) {
@@ -204,7 +200,16 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
     }
     l_run = l_run * alpha + (sf.x + sf.y);
     lb_run = lb_run * alpha + (sb.x + sb.y);
+    return true;
+  };
+  for (int j = 0; j < a.n_kv; ++j) {
+    const bool need_mask = (CAUSAL && j == a.diag) || ((j + 1) * kBN > N);
+    if (!(need_mask ? block(j, MaskTag<true>{}) : block(j, MaskTag<false>{}))) {
+      ok = false;
+      break;
+    }
   }
+
 
   if (ok) {
     ok = mbar_wait(a.pv_done, (a.n_kv - 1) & 1, ctl, kSitePvDone);

@@ -123,6 +123,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// A flag fixed at compile time that converts to bool in device code: a
+// function body inlined once with MaskTag<true> and once with
+// MaskTag<false> becomes two copies with the flag folded away.
+template <bool B>
+struct MaskTag {
+  __device__ constexpr operator bool() const { return B; }
+};
+
 // Shared control block of one CTA: an abort flag every role polls while it
 // waits, and the device status word the host reads back.
 struct WaitCtl {
