@@ -171,6 +171,13 @@ int *status_ptr() {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr long long kMaxGridX = 2147483647LL;  // largest x extent of a launch grid
+// Causal backward: pairs of mirror blocks per CTA up to this many blocks per
+// sequence (short sequences, where a CTA's fixed cost weighs most; longer
+// ones keep one block per CTA, heaviest first, which fills the last wave
+// better).  Measured with pairs at every length, B*N = 16384, H = 16, d =
+// 128: dK/dV +2..+11 % up to N = 4096 and -1..-3 % above; dQ +2..+7 % up to
+// N = 1024, even at 2048, -2..-6 % above.
+constexpr int kPairMaxBlocksKv = 32, kPairMaxBlocksQ = 16;
 
 // Host-side checks shared by both passes; no CUDA call happens before them.
 fa_status_t check_common(int B, int H, int N, int d, int causal, float scale) {
@@ -368,6 +375,8 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   // strict heaviest-first order (measured: B8 H16 N4096 +5..9 %, B1 H16
   // N16384 -2 %).
   p.head_major = (static_cast<long long>(BH) * (p.num_blk + 1) > 3040) ? 1 : 0;
+  p.pairs_kv = (causal && p.num_blk <= kPairMaxBlocksKv) ? 1 : 0;
+  p.pairs_q = (causal && p.num_blk <= kPairMaxBlocksQ) ? 1 : 0;
   fa_status_t rc = FA_OK;
   const cudaEvent_t ev[3] = {t_bwd_ev[0], t_bwd_ev[1], t_bwd_ev[2]};
   t_bwd_ev[0] = t_bwd_ev[1] = t_bwd_ev[2] = nullptr;

@@ -166,7 +166,7 @@ struct BwdLayout {
 // so P^T(t+1) is formed while dK(t) and dP^T(t+1) run, and dS^T(t+1) while
 // dV(t+1) and S^T(t+2) run.  Each product that overwrites a TMEM region
 // comes after the one that reads it (the tensor core runs them in order).
-template <int D, bool CAUSAL, bool VARLEN, int RG>
+template <int D, bool CAUSAL, bool VARLEN, int RG, bool PAIRS>
 __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -196,28 +196,40 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
-  // Tile order: causal puts the key blocks with the most query blocks
-  // (j small) first, across all heads -- or head by head when the heaviest
-  // block is short against each SM's share of the work, so that the blocks
-  // running together share their Q and dO in L2; otherwise the key blocks
-  // of one head run together.
-  int bh, jblk;
-  if (CAUSAL && !p.head_major) {
-    jblk = static_cast<int>(blockIdx.x) / p.BH;
+  // Tile order.  Causal with pairs (short sequences): a CTA takes two key
+  // blocks of one head, j and its mirror nb-1-j (one block when they
+  // coincide), which see nb + 1 query blocks together whatever j is: every
+  // CTA has the same work, and the second block's start overlaps the first
+  // one's end; the CTAs of a head run together.  Causal otherwise: one key
+  // block per CTA, the blocks with the most query blocks (j small) first,
+  // across all heads -- or head by head when the heaviest block is short
+  // against each SM's share of the work, so that the blocks running
+  // together share their Q and dO in L2.  Non-causal: the key blocks of one
+  // head run together.
+  static_assert(CAUSAL || !PAIRS, "pairs are a causal schedule");
+  constexpr bool pairs = PAIRS;
+  int bh, j0;
+  if (pairs) {
+    bh = static_cast<int>(blockIdx.x) / ((nblk + 1) / 2);
+    j0 = static_cast<int>(blockIdx.x) % ((nblk + 1) / 2);
+  } else if (CAUSAL && !p.head_major) {
+    j0 = static_cast<int>(blockIdx.x) / p.BH;
     bh = static_cast<int>(blockIdx.x) % p.BH;
   } else {
     bh = static_cast<int>(blockIdx.x) / nblk;
-    jblk = static_cast<int>(blockIdx.x) % nblk;
+    j0 = static_cast<int>(blockIdx.x) % nblk;
   }
   // The block's sequence; a block past its end (packed mode) has no work.
   const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
-  if (VARLEN && jblk * kBlk >= seq.len) return;
   const int N = seq.len, row0 = seq.start;
-  const int tma_h = bh % p.H, tma_b = VARLEN ? 0 : bh / p.H;
   const int nb = (N + kBlk - 1) / kBlk;  // blocks of this sequence
-  // Query blocks visited: causal i = j .. nb-1; otherwise all of them.
-  const int n_q = CAUSAL ? (nb - jblk) : nb;
-  const int i0 = CAUSAL ? jblk : 0;
+  if (VARLEN && (pairs ? 2 * j0 >= nb : j0 >= nb)) return;
+  const int tma_h = bh % p.H, tma_b = VARLEN ? 0 : bh / p.H;
+  const int n_items = (pairs && nb - 1 - j0 != j0) ? 2 : 1;
+  // Key block of item `it`, and the query blocks it visits: causal
+  // i = j .. nb-1; otherwise all of them.
+  auto item_j = [&](int it) { return it == 0 ? j0 : nb - 1 - j0; };
+  auto item_nq = [&](int it) { return CAUSAL ? nb - item_j(it) : nb; };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -256,33 +268,45 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-#pragma unroll
-      for (int s = 0; s < L::kSlabs; ++s) {
-        tma_load_4d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, row0 + jblk * kBlk, tma_h, tma_b);
-        tma_load_4d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, row0 + jblk * kBlk, tma_h, tma_b);
-      }
-      int issued = 0;
-      for (int t = 0; t < n_q; ++t) {
-        const int st = t % S;
-        if (!mbar_wait(&qdo_empty[st], ((t / S) & 1) ^ 1, ctl, kSiteDoEmpty)) break;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kStatBytes);
-        const int i = i0 + t;
+      // (block counters run over both items: ring stages and barrier
+      // phases carry on from the first item to the second)
+      int issued = 0, kv_issued = 0;
+      bool pok = true;
+      for (int it = 0; pok && it < n_items; ++it) {
+        const int jb = item_j(it), nq = item_nq(it), ib = CAUSAL ? jb : 0;
+        // K and V of the second item replace the first's once every
+        // product of the first is complete
+        if (it > 0 && !(pok = mbar_wait(acc_done, (it - 1) & 1, ctl, kSiteKvEmpty))) break;
+        mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
 #pragma unroll
         for (int s = 0; s < L::kSlabs; ++s) {
-          tma_load_4d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
-                      tma_b);
-          tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
-                      tma_b);
+          tma_load_4d(sK + s * kBlk * 128, &tm_k, kv_full, s * 64, row0 + jb * kBlk, tma_h, tma_b);
+          tma_load_4d(sV + s * kBlk * 128, &tm_v, kv_full, s * 64, row0 + jb * kBlk, tma_h, tma_b);
         }
-        const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + static_cast<size_t>(i) * kBlk;
-        bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
-        bulk_load(sStats + st * L::kStatBytes + kBlk * 4, p.delta + srow, kBlk * 4, &qdo_full[st]);
-        issued = t + 1;
+        kv_issued = it + 1;
+        for (int t = 0; t < nq; ++t) {
+          const int g = issued, st = g % S;
+          if (!(pok = mbar_wait(&qdo_empty[st], ((g / S) & 1) ^ 1, ctl, kSiteDoEmpty))) break;
+          mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kStatBytes);
+          const int i = ib + t;
+#pragma unroll
+          for (int s = 0; s < L::kSlabs; ++s) {
+            tma_load_4d(sQ + st * L::kTile + s * kBlk * 128, &tm_q, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
+                        tma_b);
+            tma_load_4d(sDO + st * L::kTile + s * kBlk * 128, &tm_do, &qdo_full[st], s * 64, row0 + i * kBlk, tma_h,
+                        tma_b);
+          }
+          const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + static_cast<size_t>(i) * kBlk;
+          bulk_load(sStats + st * L::kStatBytes, p.lse2 + srow, kBlk * 4, &qdo_full[st]);
+          bulk_load(sStats + st * L::kStatBytes + kBlk * 4, p.delta + srow, kBlk * 4, &qdo_full[st]);
+          issued = g + 1;
+        }
       }
       // Every copy issued lands before this thread leaves, whatever the
       // other roles do (bounded waits; in a normal run they are done).
-      mbar_drain(kv_full, 0);
+      // A K/V load is issued only after the previous one was consumed, so
+      // the last one's phase covers both.
+      if (kv_issued > 0) mbar_drain(kv_full, (kv_issued - 1) & 1);
       for (int t = (issued > S ? issued - S : 0); t < issued; ++t) mbar_drain(&qdo_full[t % S], (t / S) & 1);
     }
   } else if (warp == 1) {
@@ -317,47 +341,57 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
         tc_commit(s_full);
       };
 
-      bool ok = mbar_wait(kv_full, 0, ctl, kSiteKvFull) && mbar_wait(&qdo_full[0], 0, ctl, kSiteDoFull);
-      if (ok) {
+      // g: block counter over both items (ring stage g % S, phases g & 1)
+      bool ok = true;
+      for (int it = 0, g0 = 0; ok && it < n_items; g0 += item_nq(it), ++it) {
+        const int nq = item_nq(it);
+        // (the second item's first S^T, dP^T overwrite columns the first
+        // item's last dV, dK read: issued after them, they run after them)
+        ok = mbar_wait(kv_full, it & 1, ctl, kSiteKvFull) && mbar_wait(&qdo_full[g0 % S], (g0 / S) & 1, ctl, kSiteDoFull);
+        if (!ok) break;
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int t = 0; ok && t < n_q; ++t) {
-        const int st = t % S;
-        const bool more = t + 1 < n_q;
-        // dV += P^T dO_t   (P^T from TMEM; dO_t is MN-major over d)
-        if (!(ok = mbar_wait(p_ready, t & 1, ctl, kSitePReady))) break;
-        tc_fence_after();
-        {
-          const uint64_t bdo = do_mn(t);
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)  // P^T of queries [c g, c g + c) sits at columns c g.. (c = kKvCols)
-            mma_ts(tDV, tS + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8, desc_add(bdo, mnmajor_step(kk)),
-                   kIdescKV, (t > 0 || kk > 0));
-        }
-        // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
-        // first, reads P^T(t) before S^T(t+1) overwrites it
-        if (more) {
-          if (!(ok = mbar_wait(&qdo_full[(t + 1) % S], ((t + 1) / S) & 1, ctl, kSiteDoFull))) break;
+        issue_s(g0);
+        issue_dp(g0);
+        for (int t = 0; ok && t < nq; ++t) {
+          const int g = g0 + t;
+          const bool more = t + 1 < nq;
+          // dV += P^T dO_t   (P^T from TMEM; dO_t is MN-major over d).  The
+          // item's first dV overwrites the accumulator: its rows arrive on
+          // p_ready only after storing the previous item's dV and dK.
+          if (!(ok = mbar_wait(p_ready, g & 1, ctl, kSitePReady))) break;
           tc_fence_after();
-          issue_s(t + 1);
-        }
-        // dK += dS^T Q_t (dS^T from TMEM over the dP^T columns; Q_t MN-major
-        // over d), then dP^T(t+1) over them once dK(t) has read them
-        if (!(ok = mbar_wait(ds_ready, t & 1, ctl, kSiteDsReady))) break;
-        tc_fence_after();
-        {
-          const uint64_t bq = q_mn(t);
+          {
+            const uint64_t bdo = do_mn(g);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS^T of queries [c g, c g + c) sits at columns 128 + c g..
-            mma_ts(tDK, tDP + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8, desc_add(bq, mnmajor_step(kk)),
-                   kIdescKV, (t > 0 || kk > 0));
+            for (int kk = 0; kk < kBlk / 16; ++kk)  // P^T of queries [c g, c g + c) sits at columns c g.. (c = kKvCols)
+              mma_ts(tDV, tS + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8,
+                     desc_add(bdo, mnmajor_step(kk)), kIdescKV, (t > 0 || kk > 0));
+          }
+          // S^T(t+1): the rows have read S^T(t) (p_ready) and dV(t), issued
+          // first, reads P^T(t) before S^T(t+1) overwrites it
+          if (more) {
+            if (!(ok = mbar_wait(&qdo_full[(g + 1) % S], ((g + 1) / S) & 1, ctl, kSiteDoFull))) break;
+            tc_fence_after();
+            issue_s(g + 1);
+          }
+          // dK += dS^T Q_t (dS^T from TMEM over the dP^T columns; Q_t MN-major
+          // over d), then dP^T(t+1) over them once dK(t) has read them
+          if (!(ok = mbar_wait(ds_ready, g & 1, ctl, kSiteDsReady))) break;
+          tc_fence_after();
+          {
+            const uint64_t bq = q_mn(g);
+#pragma unroll
+            for (int kk = 0; kk < kBlk / 16; ++kk)  // dS^T of queries [c g, c g + c) sits at columns 128 + c g..
+              mma_ts(tDK, tDP + (kk / (kKvCols / 16)) * kKvCols + (kk % (kKvCols / 16)) * 8,
+                     desc_add(bq, mnmajor_step(kk)), kIdescKV, (t > 0 || kk > 0));
+          }
+          tc_commit(&qdo_empty[g % S]);
+          if (more) issue_dp(g + 1);
         }
-        tc_commit(&qdo_empty[st]);
-        if (more) issue_dp(t + 1);
+        // the item's dV, dK are complete (the rows store them), and K, V
+        // are free for the next item (the producer waits on this too)
+        if (ok) tc_commit(acc_done);
       }
-      if (ok) tc_commit(acc_done);
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
@@ -366,130 +400,133 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
     const int grp = (warp >> 2) - 1;  // query columns [kKvCols grp, kKvCols (grp + 1))
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the block
-    const int key = jblk * kBlk + r;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
-    const bool key_ok = key < N;
     const int c0 = grp * kKvCols;  // first query column of this quarter
     bool ok = true;
 
-    for (int t = 0; t < n_q; ++t) {
-      const int i = i0 + t;
-      // per-query statistics of this block, in shared memory with Q and dO
-      // (same address in every thread: broadcast reads)
-      const float *stats = reinterpret_cast<const float *>(sStats + (t % S) * L::kStatBytes);
-      const float4 *lse4 = reinterpret_cast<const float4 *>(stats + c0);
-      const float4 *del4 = reinterpret_cast<const float4 *>(stats + kBlk + c0);
-      const bool diag = CAUSAL && (i == jblk);
+    for (int it = 0, g0 = 0; ok && it < n_items; g0 += item_nq(it), ++it) {
+      const int jblk = item_j(it), n_q = item_nq(it), i0 = CAUSAL ? jblk : 0;
+      const int key = jblk * kBlk + r;
+      const bool key_ok = key < N;
+      for (int t = 0; t < n_q; ++t) {
+        const int i = i0 + t, g = g0 + t;  // g: block counter over both items
+        // per-query statistics of this block, in shared memory with Q and dO
+        // (same address in every thread: broadcast reads)
+        const float *stats = reinterpret_cast<const float *>(sStats + (g % S) * L::kStatBytes);
+        const float4 *lse4 = reinterpret_cast<const float4 *>(stats + c0);
+        const float4 *del4 = reinterpret_cast<const float4 *>(stats + kBlk + c0);
+        const bool diag = CAUSAL && (i == jblk);
 
-      // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + kKvCols / 2).
-      // (The stage's copies are complete once S^T(t) is; the rows wait on
-      // them too so that the statistics' copy is visible to their loads.
-      // The stage cannot be refilled before ds_ready(t).)
-      ok = mbar_wait(s_full, t & 1, ctl, kSiteSFull) &&
-           mbar_wait(&qdo_full[t % S], (t / S) & 1, ctl, kSiteDoFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // P^T of this quarter row in fp32 pairs (kept for phase 2) and as bf16
-      // pairs in TMEM.  Key rows past N (zero rows of K, so S = 0) get a
-      // finite P that only reaches their own dV, dK rows, which are not
-      // stored: no mask needed.
-      constexpr int kCh = kKvCols / 32;  // 32-column chunks per row thread
-      float2 pf[kKvCols / 2];
-      {
-        uint32_t sva[kCh][32];
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(sva[ch]);
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) {
-          const uint32_t(&sv)[32] = sva[ch];
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int qh = ch * 32 + e;  // query column within this thread's columns
-            const float4 l4 = lse4[qh / 4];
-            const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                     make_float2(c, c), make_float2(-l4.x, -l4.y));
-            const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
-                                     make_float2(c, c), make_float2(-l4.z, -l4.w));
-            float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
-            if (diag) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
+        // Phase 1: P^T = exp2(S^T c - lse2) -> bf16 over S^T columns [c0, c0 + kKvCols / 2).
+        // (The stage's copies are complete once S^T(t) is; the rows wait on
+        // them too so that the statistics' copy is visible to their loads.
+        // The stage cannot be refilled before ds_ready(t).)
+        ok = mbar_wait(s_full, g & 1, ctl, kSiteSFull) &&
+             mbar_wait(&qdo_full[g % S], (g / S) & 1, ctl, kSiteDoFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // P^T of this quarter row in fp32 pairs (kept for phase 2) and as bf16
+        // pairs in TMEM.  Key rows past N (zero rows of K, so S = 0) get a
+        // finite P that only reaches their own dV, dK rows, which are not
+        // stored: no mask needed.
+        constexpr int kCh = kKvCols / 32;  // 32-column chunks per row thread
+        float2 pf[kKvCols / 2];
+        {
+          uint32_t sva[kCh][32];
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(sva[ch]);
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) {
+            const uint32_t(&sv)[32] = sva[ch];
+            uint32_t pk[16];
+  #pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const int qh = ch * 32 + e;  // query column within this thread's columns
+              const float4 l4 = lse4[qh / 4];
+              const float2 x01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                       make_float2(c, c), make_float2(-l4.x, -l4.y));
+              const float2 x23 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                       make_float2(c, c), make_float2(-l4.z, -l4.w));
+              float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+              if (diag) {
+  #pragma unroll
+                for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
+              }
+              pf[qh / 2] = make_float2(pr[0], pr[1]);
+              pf[qh / 2 + 1] = make_float2(pr[2], pr[3]);
+              pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
+              pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
             }
-            pf[qh / 2] = make_float2(pr[0], pr[1]);
-            pf[qh / 2 + 1] = make_float2(pr[2], pr[3]);
-            pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
-            pk[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+            tmem_st16(tS + c0 + ch * 16, pk);  // over scores of this thread's columns, already read
           }
-          tmem_st16(tS + c0 + ch * 16, pk);  // over scores of this thread's columns, already read
         }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(p_ready);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(p_ready);
 
-      // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 pairs over this quarter's
-      // own, already read, dP^T columns.
-      ok = mbar_wait(dp_full, t & 1, ctl, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      {
-        uint32_t dpa[kCh][32];
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(dpa[ch]);
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch) {
-          const uint32_t(&dpv)[32] = dpa[ch];
-          uint32_t dk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int qh = ch * 32 + e;
-            const float4 d4 = del4[qh / 4];
-            const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
-                                     make_float2(-d4.x, -d4.y));
-            const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
-                                     make_float2(-d4.z, -d4.w));
-            const float2 ds01 = fmul2(pf[qh / 2], g01);
-            const float2 ds23 = fmul2(pf[qh / 2 + 1], g23);
-            dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
-            dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
-          }
-          tmem_st16(tDP + c0 + ch * 16, dk);
+        // Phase 2: dS^T = P^T o (dP^T - D) -> bf16 pairs over this quarter's
+        // own, already read, dP^T columns.
+        ok = mbar_wait(dp_full, g & 1, ctl, kSiteSFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        {
+          uint32_t dpa[kCh][32];
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(dpa[ch]);
+  #pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) {
+            const uint32_t(&dpv)[32] = dpa[ch];
+            uint32_t dk[16];
+  #pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const int qh = ch * 32 + e;
+              const float4 d4 = del4[qh / 4];
+              const float2 g01 = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                       make_float2(-d4.x, -d4.y));
+              const float2 g23 = fadd2(make_float2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                       make_float2(-d4.z, -d4.w));
+              const float2 ds01 = fmul2(pf[qh / 2], g01);
+              const float2 ds23 = fmul2(pf[qh / 2 + 1], g23);
+              dk[e / 2] = pack_bf16x2(ds01.x, ds01.y);
+              dk[e / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
+            }
+            tmem_st16(tDP + c0 + ch * 16, dk);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(ds_ready);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(ds_ready);
-    }
-    // epilogues: the first half of the row groups writes dV, the second dK
-    // (scale applied here), each group a D / (RG / 2) column slice
-    if (ok) {
-      ok = mbar_wait(acc_done, 0, ctl, kSiteMmaDone);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      constexpr int kW = D / (RG / 2);  // columns per group
-      const int col = (grp % (RG / 2)) * kW;
-      if (grp < RG / 2)
-        store_acc_row<kW>(tmem + kColDV + lane_base + col, p.dv + row_offset(p.sdv, bh, p.H, row0 + key) + col,
-                          key_ok, 1.0f);
-      else
-        store_acc_row<kW>(tmem + kColDK + lane_base + col, p.dk + row_offset(p.sdk, bh, p.H, row0 + key) + col,
-                          key_ok, p.scale);
-    }
+      // epilogues: the first half of the row groups writes dV, the second dK
+      // (scale applied here), each group a D / (RG / 2) column slice
+      if (ok) {
+        ok = mbar_wait(acc_done, it & 1, ctl, kSiteMmaDone);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        constexpr int kW = D / (RG / 2);  // columns per group
+        const int col = (grp % (RG / 2)) * kW;
+        if (grp < RG / 2)
+          store_acc_row<kW>(tmem + kColDV + lane_base + col, p.dv + row_offset(p.sdv, bh, p.H, row0 + key) + col,
+                            key_ok, 1.0f);
+        else
+          store_acc_row<kW>(tmem + kColDK + lane_base + col, p.dk + row_offset(p.sdk, bh, p.H, row0 + key) + col,
+                            key_ok, p.scale);
+      }
+    }  // items
   }
 
   tc_fence_before();
@@ -530,7 +567,7 @@ struct DqLayout {
 // S(j+2) runs; dP(j+1) overwrites dS(j) after dQ(j) has read it (the tensor
 // core runs the products in order).  K(j) is read by S(j) and, last, by
 // dQ(j); the third K stage lets K(j+2) load while dQ(j) still holds K(j).
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -562,26 +599,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
-  // Tile order: causal puts the query blocks with the most key blocks
-  // (i large) first; otherwise the query blocks of one head run together.
-  int bh, iblk;
-  if (CAUSAL && !p.head_major) {
-    iblk = nblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
+  // Tile order.  Causal with pairs (short sequences): a CTA takes the
+  // query blocks nb-1-i and i of one head (one block when they coincide),
+  // which see nb + 1 key blocks together; the CTAs of a head run together.
+  // Causal otherwise: the query blocks with the most key blocks (i large)
+  // first, across all heads or head by head (as the dK/dV kernel).
+  // Non-causal: the query blocks of one head run together.
+  static_assert(CAUSAL || !PAIRS, "pairs are a causal schedule");
+  constexpr bool pairs = PAIRS;
+  int bh, i0;  // i0: the first item's query block (pairs: its mirror's index)
+  if (pairs) {
+    bh = static_cast<int>(blockIdx.x) / ((nblk + 1) / 2);
+    i0 = static_cast<int>(blockIdx.x) % ((nblk + 1) / 2);
+  } else if (CAUSAL && !p.head_major) {
+    i0 = nblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
     bh = static_cast<int>(blockIdx.x) % p.BH;
   } else if (CAUSAL) {  // head by head, heaviest query blocks first
     bh = static_cast<int>(blockIdx.x) / nblk;
-    iblk = nblk - 1 - static_cast<int>(blockIdx.x) % nblk;
+    i0 = nblk - 1 - static_cast<int>(blockIdx.x) % nblk;
   } else {
     bh = static_cast<int>(blockIdx.x) / nblk;
-    iblk = static_cast<int>(blockIdx.x) % nblk;
+    i0 = static_cast<int>(blockIdx.x) % nblk;
   }
   // The block's sequence; a block past its end (packed mode) has no work.
   const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
-  if (VARLEN && iblk * kBlk >= seq.len) return;
   const int N = seq.len, row0 = seq.start;
+  const int nb = (N + kBlk - 1) / kBlk;  // blocks of this sequence
+  if (VARLEN && (pairs ? 2 * i0 >= nb : i0 >= nb)) return;
   const int tma_h = bh % p.H, tma_b = VARLEN ? 0 : bh / p.H;
-  const int nb = (N + kBlk - 1) / kBlk;                  // blocks of this sequence
-  const int n_kv = CAUSAL ? (iblk + 1) : nb;  // key blocks 0 .. n_kv-1
+  const int n_items = (pairs && nb - 1 - i0 != i0) ? 2 : 1;
+  // Query block of item `it` (pairs: the heavier one first) and the key
+  // blocks 0 .. n_kv-1 it visits.
+  auto item_i = [&](int it) { return pairs ? (it == 0 ? nb - 1 - i0 : i0) : i0; };
+  auto item_nkv = [&](int it) { return CAUSAL ? item_i(it) + 1 : nb; };
 
   if (threadIdx.x == 0) {
     mbar_init(do_ready, kRowWarps);
@@ -619,30 +669,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // the K ring
       tma_prefetch_desc(&tm_k);
+      // (the ring runs over both items' key blocks: stage g % SK)
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % SK;
-        if (!mbar_wait(&k_empty[st], ((j / SK) & 1) ^ 1, ctl, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::kTile);
+      bool pok = true;
+      for (int it = 0; pok && it < n_items; ++it)
+        for (int j = 0; j < item_nkv(it); ++j) {
+          const int g = issued, st = g % SK;
+          if (!(pok = mbar_wait(&k_empty[st], ((g / SK) & 1) ^ 1, ctl, kSiteKEmpty))) break;
+          mbar_arrive_expect_tx(&k_full[st], L::kTile);
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
-        issued = j + 1;
-      }
+          for (int s = 0; s < L::kSlabs; ++s)
+            tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBlk, tma_h,
+                        tma_b);
+          issued = g + 1;
+        }
       for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
     } else if (lane == 1) {
       // the V ring
       tma_prefetch_desc(&tm_v);
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % SV;
-        if (!mbar_wait(&v_empty[st], ((j / SV) & 1) ^ 1, ctl, kSiteVEmpty)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::kTile);
+      bool pok = true;
+      for (int it = 0; pok && it < n_items; ++it)
+        for (int j = 0; j < item_nkv(it); ++j) {
+          const int g = issued, st = g % SV;
+          if (!(pok = mbar_wait(&v_empty[st], ((g / SV) & 1) ^ 1, ctl, kSiteVEmpty))) break;
+          mbar_arrive_expect_tx(&v_full[st], L::kTile);
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBlk, tma_h, tma_b);
-        issued = j + 1;
-      }
+          for (int s = 0; s < L::kSlabs; ++s)
+            tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBlk, tma_h,
+                        tma_b);
+          issued = g + 1;
+        }
       for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&v_full[j % SV], (j / SV) & 1);
     }
   } else if (warp == 1) {
@@ -673,48 +730,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts(tDP, tDO + kk * 8, desc_add(bv, kmajor_step(kk, kBlk)), kIdescS, kk > 0);
       };
 
-      bool ok = mbar_wait(&k_full[0], 0, ctl, kSiteKFull) &&
-                mbar_wait(&v_full[0], 0, ctl, kSiteVFull) && mbar_wait(do_ready, 0, ctl, kSiteDoFull);
-      if (ok) {
+      // g: key-block counter over both items (ring stages, barrier phases)
+      bool ok = true;
+      for (int it = 0, g0 = 0; ok && it < n_items; g0 += item_nkv(it), ++it) {
+        const int n_kv = item_nkv(it);
+        // the item's Q and dO in TMEM (written by the rows once the previous
+        // item's products were complete and its dQ was read out)
+        ok = mbar_wait(&k_full[g0 % SK], (g0 / SK) & 1, ctl, kSiteKFull) &&
+             mbar_wait(&v_full[g0 % SV], (g0 / SV) & 1, ctl, kSiteVFull) && mbar_wait(do_ready, it & 1, ctl, kSiteDoFull);
+        if (!ok) break;
         tc_fence_after();
-        issue_s(0);
-        const uint64_t bv = v_kmaj(0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
-        tc_commit(dp_full);
-        tc_commit(&v_empty[0]);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const bool more = j + 1 < n_kv;
-        if (more) {
-          // S(j+1) once the rows have read S(j)
-          if (!(ok = mbar_wait(&k_full[(j + 1) % SK], ((j + 1) / SK) & 1, ctl, kSiteKFull))) break;
-          if (!(ok = mbar_wait(s_free, j & 1, ctl, kSiteSFull))) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        // dQ += dS K_j (dS from TMEM over the dP columns; K_j MN-major over
-        // d) once the rows have written dS(j), then dP(j+1) over it
-        if (!(ok = mbar_wait(ds_ready, j & 1, ctl, kSiteDsReady))) break;
-        if (more && !(ok = mbar_wait(&v_full[(j + 1) % SV], ((j + 1) / SV) & 1, ctl, kSiteVFull))) break;
-        tc_fence_after();
+        issue_s(g0);
         {
-          const uint64_t bk = k_mn(j);
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)  // dS of keys [64h, 64h+64) sits at columns 128 + 64h..
-            mma_ts(tDQ, tDP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bk, mnmajor_step(kk)), kIdescQ,
-                   (j > 0 || kk > 0));
-        }
-        tc_commit(&k_empty[j % SK]);
-        if (more) {
-          const uint64_t bv = v_kmaj(j + 1);
+          const uint64_t bv = v_kmaj(g0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
-          tc_commit(dp_full);
-          tc_commit(&v_empty[(j + 1) % SV]);
         }
+        tc_commit(dp_full);
+        tc_commit(&v_empty[g0 % SV]);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int g = g0 + j;
+          const bool more = j + 1 < n_kv;
+          if (more) {
+            // S(j+1) once the rows have read S(j)
+            if (!(ok = mbar_wait(&k_full[(g + 1) % SK], ((g + 1) / SK) & 1, ctl, kSiteKFull))) break;
+            if (!(ok = mbar_wait(s_free, g & 1, ctl, kSiteSFull))) break;
+            tc_fence_after();
+            issue_s(g + 1);
+          }
+          // dQ += dS K_j (dS from TMEM over the dP columns; K_j MN-major over
+          // d) once the rows have written dS(j), then dP(j+1) over it
+          if (!(ok = mbar_wait(ds_ready, g & 1, ctl, kSiteDsReady))) break;
+          if (more && !(ok = mbar_wait(&v_full[(g + 1) % SV], ((g + 1) / SV) & 1, ctl, kSiteVFull))) break;
+          tc_fence_after();
+          {
+            const uint64_t bk = k_mn(g);
+#pragma unroll
+            for (int kk = 0; kk < kBlk / 16; ++kk)  // dS of keys [64h, 64h+64) sits at columns 128 + 64h..
+              mma_ts(tDQ, tDP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(bk, mnmajor_step(kk)), kIdescQ,
+                     (j > 0 || kk > 0));
+          }
+          tc_commit(&k_empty[g % SK]);
+          if (more) {
+            const uint64_t bv = v_kmaj(g + 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) dp_step(bv, kk);
+            tc_commit(dp_full);
+            tc_commit(&v_empty[(g + 1) % SV]);
+          }
+        }
+        // the item's dQ is complete, and its Q, dO columns are free
+        if (ok) tc_commit(dq_done);
       }
-      if (ok) tc_commit(dq_done);
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
@@ -723,123 +790,130 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp >> 2) - 1;  // key columns [64 half, 64 half + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // query row within the block
-    const int qrow = iblk * kBlk + r;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + kColS + lane_base, tDP = tmem + kColDP + lane_base;
     const float c = p.scale_log2;
-    const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + qrow;
-    const float lse2 = p.lse2[srow];  // +inf on padding rows: P = 0
-    const float dlt = p.delta[srow];
-    const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
     const int c0 = half * 64;  // first key column of this half
     bool ok = true;
 
-    // Q and dO rows -> TMEM (bf16 pairs over D/2 columns each): the A
-    // operands of S and dP.  The two halves share the 64-element pieces.
-    {
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(m ? p.dout + row_offset(p.sdo, bh, p.H, row0 + qrow)
-                                                             : p.q + row_offset(p.sq, bh, p.H, row0 + qrow));
-        const uint32_t col = m ? kColDO : kColQ;
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          if (((hh + m) & 1) != half) continue;
-          uint32_t v[32];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 x = qrow < N ? src[hh * 8 + u] : make_uint4(0, 0, 0, 0);
-            v[4 * u] = x.x;
-            v[4 * u + 1] = x.y;
-            v[4 * u + 2] = x.z;
-            v[4 * u + 3] = x.w;
-          }
-          tmem_st32(tmem + col + lane_base + hh * 32, v);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(do_ready);
-    }
+    for (int it = 0, g0 = 0; ok && it < n_items; g0 += item_nkv(it), ++it) {
+      const int iblk = item_i(it), n_kv = item_nkv(it);
+      const int qrow = iblk * kBlk + r;
+      const size_t srow = static_cast<size_t>(bh) * nblk * kBlk + qrow;
+      const float lse2 = p.lse2[srow];  // +inf on padding rows: P = 0
+      const float dlt = p.delta[srow];
+      const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
 
-    for (int j = 0; j < n_kv; ++j) {
-      const bool diag = CAUSAL && (j == iblk);
-      // packed mode: keys past the sequence are the next sequence's rows and
-      // must get P = 0 (batched mode: they are zero rows of K and V, whose
-      // dS K adds nothing)
-      const int klim = N - 1 - j * kBlk;  // last key column of this block inside the sequence
-      const bool kmask = VARLEN && klim < kBlk - 1;
-      // Phase 1: P = exp2(S c - lse2) for this half of the keys, kept as bf16 pairs.
-      ok = mbar_wait(s_full, j & 1, ctl, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float2 pf[32];  // P of this half row (fp32 pairs), kept for phase 2
-      uint32_t sva[2][32];
+      // Q and dO rows -> TMEM (bf16 pairs over D/2 columns each): the A
+      // operands of S and dP.  The two halves share the 64-element pieces.
+      // (A second item overwrites the first's once its products are complete:
+      // these rows have waited for dq_done and stored its dQ.)
+      {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
+        for (int m = 0; m < 2; ++m) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(m ? p.dout + row_offset(p.sdo, bh, p.H, row0 + qrow)
+                                                               : p.q + row_offset(p.sq, bh, p.H, row0 + qrow));
+          const uint32_t col = m ? kColDO : kColQ;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
-      tc_fence_before();
-      warp_arrive(s_free);  // S is in registers: the next S may overwrite it
+          for (int hh = 0; hh < D / 64; ++hh) {
+            if (((hh + m) & 1) != half) continue;
+            uint32_t v[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const uint32_t(&sv)[32] = sva[ch];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
-          float p0 = ex2(x.x), p1 = ex2(x.y);
-          if (diag || kmask) {  // key kc visible to query r iff kc <= r (causal) and kc < N
-            const int lim = diag ? min(r, klim) : klim;
-            p0 = (c0 + ch * 32 + e <= lim) ? p0 : 0.0f;
-            p1 = (c0 + ch * 32 + e + 1 <= lim) ? p1 : 0.0f;
+            for (int u = 0; u < 8; ++u) {
+              const uint4 x = qrow < N ? src[hh * 8 + u] : make_uint4(0, 0, 0, 0);
+              v[4 * u] = x.x;
+              v[4 * u + 1] = x.y;
+              v[4 * u + 2] = x.z;
+              v[4 * u + 3] = x.w;
+            }
+            tmem_st32(tmem + col + lane_base + hh * 32, v);
           }
-          pf[ch * 16 + e / 2] = make_float2(p0, p1);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(do_ready);
       }
 
-      // Phase 2: dS = P o (dP - D) -> bf16 pairs over this half's own,
-      // already read, dP columns (dQ(j-1) has read dS(j-1) from there: it
-      // ran before dP(j)).
-      ok = mbar_wait(dp_full, j & 1, ctl, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t dpa[2][32];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(dpa[ch]);
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const uint32_t(&dpv)[32] = dpa[ch];
-        uint32_t dsv[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 g = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd);
-          const float2 ds = fmul2(pf[ch * 16 + e / 2], g);
-          dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
+      for (int j = 0; j < n_kv; ++j) {
+        const int gb = g0 + j;  // key-block counter over both items
+        const bool diag = CAUSAL && (j == iblk);
+        // packed mode: keys past the sequence are the next sequence's rows and
+        // must get P = 0 (batched mode: they are zero rows of K and V, whose
+        // dS K adds nothing)
+        const int klim = N - 1 - j * kBlk;  // last key column of this block inside the sequence
+        const bool kmask = VARLEN && klim < kBlk - 1;
+        // Phase 1: P = exp2(S c - lse2) for this half of the keys, kept as bf16 pairs.
+        ok = mbar_wait(s_full, gb & 1, ctl, kSiteSFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-        tmem_st16(tDP + c0 + ch * 16, dsv);
+        tc_fence_after();
+        float2 pf[32];  // P of this half row (fp32 pairs), kept for phase 2
+        uint32_t sva[2][32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
+        tc_fence_before();
+        warp_arrive(s_free);  // S is in registers: the next S may overwrite it
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const uint32_t(&sv)[32] = sva[ch];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
+            float p0 = ex2(x.x), p1 = ex2(x.y);
+            if (diag || kmask) {  // key kc visible to query r iff kc <= r (causal) and kc < N
+              const int lim = diag ? min(r, klim) : klim;
+              p0 = (c0 + ch * 32 + e <= lim) ? p0 : 0.0f;
+              p1 = (c0 + ch * 32 + e + 1 <= lim) ? p1 : 0.0f;
+            }
+            pf[ch * 16 + e / 2] = make_float2(p0, p1);
+          }
+        }
+
+        // Phase 2: dS = P o (dP - D) -> bf16 pairs over this half's own,
+        // already read, dP columns (dQ(j-1) has read dS(j-1) from there: it
+        // ran before dP(j)).
+        ok = mbar_wait(dp_full, gb & 1, ctl, kSiteSFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dpa[2][32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(dpa[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const uint32_t(&dpv)[32] = dpa[ch];
+          uint32_t dsv[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 g = fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd);
+            const float2 ds = fmul2(pf[ch * 16 + e / 2], g);
+            dsv[e / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+          tmem_st16(tDP + c0 + ch * 16, dsv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(ds_ready);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(ds_ready);
-    }
-    // dQ epilogue (the scale applied here): each half writes D/2 columns
-    if (ok) {
-      ok = mbar_wait(dq_done, 0, ctl, kSiteMmaDone);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      store_acc_row<D / 2>(tmem + kColDQ + lane_base + half * (D / 2),
-                           p.dq + row_offset(p.sdq, bh, p.H, row0 + qrow) + half * (D / 2), qrow < N, p.scale);
-    }
+      // dQ epilogue (the scale applied here): each half writes D/2 columns
+      if (ok) {
+        ok = mbar_wait(dq_done, it & 1, ctl, kSiteMmaDone);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        store_acc_row<D / 2>(tmem + kColDQ + lane_base + half * (D / 2),
+                             p.dq + row_offset(p.sdq, bh, p.H, row0 + qrow) + half * (D / 2), qrow < N, p.scale);
+      }
+    }  // items
   }
 
   tc_fence_before();
@@ -897,9 +971,19 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
       <<<static_cast<unsigned>(pre_blocks < kPreGridMax ? pre_blocks : kPreGridMax), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_blk);
+  // one CTA per block, or (causal with pairs) per pair of mirror blocks
+  const unsigned grid_kv = static_cast<unsigned>(p.BH) *
+                           static_cast<unsigned>((CAUSAL && p.pairs_kv) ? (p.num_blk + 1) / 2 : p.num_blk);
+  const unsigned grid_q = static_cast<unsigned>(p.BH) *
+                          static_cast<unsigned>((CAUSAL && p.pairs_q) ? (p.num_blk + 1) / 2 : p.num_blk);
   // (long non-causal heads: four row groups; causal: two, see KvRows)
   constexpr int RG = CAUSAL ? 2 : 4;
+  // the schedule is a template parameter: the one-block kernels carry no
+  // loop over items (measured 3-4 % faster than a run-time flag)
+  const auto kern_kv = (CAUSAL && p.pairs_kv) ? fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, CAUSAL>
+                                              : fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, false>;
+  const auto kern_q = (CAUSAL && p.pairs_q) ? fa_bwd_dq_kernel<D, CAUSAL, VARLEN, CAUSAL>
+                                            : fa_bwd_dq_kernel<D, CAUSAL, VARLEN, false>;
   if (concurrent && !ev) {
     // The dQ kernel reads only the inputs and the pre-kernel's statistics,
     // so it runs on a side stream next to the dK/dV kernel: each grid is
@@ -910,21 +994,21 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     if ((e = side_stream(&side)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(side->fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
-    e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG>, grid, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk,
-                    tv, tdo, p, stream);
+    e = launch_main(kern_kv, grid_kv, KvRows<RG>::kThreads, L::kSmemRequest, tq,
+                    tk, tv, tdo, p, stream);
     if (e != cudaSuccess) return e;
-    e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
+    e = launch_main(kern_q, grid_q, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
                     p, side->stream);
     if (e != cudaSuccess) return e;
     if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
     return cudaStreamWaitEvent(stream, side->join, 0);
   }
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG>, grid, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk, tv,
-                  tdo, p, stream);
+  e = launch_main(kern_kv, grid_kv, KvRows<RG>::kThreads, L::kSmemRequest, tq, tk,
+                  tv, tdo, p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-  e = launch_main(fa_bwd_dq_kernel<D, CAUSAL, VARLEN>, grid, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
+  e = launch_main(kern_q, grid_q, kThreads, DqLayout<D>::kSmemRequest, tq, tk, tv, tdo,
                   p, stream);
   if (e != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;

@@ -98,6 +98,8 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int head_major;             // causal: order the blocks head by head (heaviest first inside a head)
+  int pairs_kv, pairs_q;      // causal: one CTA per pair of mirror blocks (j, nb-1-j) of a head in the
+                              // dK/dV kernel, in the dQ kernel
 };
 
 // Decode forward: Nq (<= 8) query rows per head against Nk cached keys.
