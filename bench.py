@@ -765,14 +765,17 @@ def e2e_leg(pb, args, world):
     pipe_steps(steps)
     b2.record(sc)
     torch.cuda.synchronize()
-    value, _ = aggregate_throughput(flops, steps, a2.elapsed_time(b2), world, "cuda")
+    pipe_value, _ = aggregate_throughput(flops, steps, a2.elapsed_time(b2), world, "cuda")
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in sets[0][3]) + sets[0][4].numel() * 4
-    return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "pipelined": True, "sequential_value": seq_value,
-            "note": "pipelined over three buffer sets: each step's host->device copy overlaps earlier steps' "
-                    "compute and its device->host copy later steps', on their own streams; sequential_value: "
-                    "copy in, compute, copy out on one stream"}
+    # the better of the two schedules (a copy-bound workload, whose copies
+    # cannot hide behind its compute, may do better on one stream)
+    return {"value": max(pipe_value, seq_value), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "pipelined": pipe_value >= seq_value,
+            "pipelined_value": pipe_value, "sequential_value": seq_value,
+            "note": "value: the better of two schedules. pipelined_value: over three buffer sets, each step's "
+                    "host->device copy overlaps earlier steps' compute and its device->host copy later steps', "
+                    "on their own streams; sequential_value: copy in, compute, copy out on one stream"}
 
 
 def run_sweep(args):
