@@ -165,7 +165,7 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
           p2 = (k0 + 2 <= lim) ? p2 : 0.0f;
           p3 = (k0 + 3 <= lim) ? p3 : 0.0f;
         }
-        pk[q4 * 8 + i / 4] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+        pk[q4 * 8 + i / 4] = pack_e4m3x4(p0, p1, p2, p3);
         sfq = fadd2(sfq, fadd2(make_float2(p0, p1), make_float2(p2, p3)));
       }
       sf = fadd2(sf, sfq);
@@ -195,8 +195,7 @@ __device__ __forceinline__ void softmax_tile_f8(const F8SoftmaxArgs &a, const Fp
     float2 sb = make_float2(0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < 32; ++w) {
-      sb = add_e4m3x2_f32(sb, static_cast<uint16_t>(pk[w] & 0xffffu));
-      sb = add_e4m3x2_f32(sb, static_cast<uint16_t>(pk[w] >> 16));
+      sb = add_e4m3x4_f32(sb, pk[w]);
     }
     l_run = l_run * alpha + (sf.x + sf.y);
     lb_run = lb_run * alpha + (sb.x + sb.y);

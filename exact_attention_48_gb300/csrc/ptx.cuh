@@ -374,24 +374,35 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Two fp32 values rounded to e4m3 (nearest, ties to even, saturated to the
-// finite range) and packed: lo in the low byte, hi in the high byte.
-__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// Four fp32 values rounded to e4m3 (nearest, ties to even, saturated to
+// the finite range) in one 32-bit word: a in the lowest byte, then b, c, d.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
   return r;
 }
 
-// acc.x += the e4m3 value in the low byte of b, acc.y += the high byte's
-// (decoded exactly through f16, added with one rounding each).
-__device__ __forceinline__ float2 add_e4m3x2_f32(float2 acc, uint16_t b) {
-  asm("{\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
-      "cvt.rn.f16x2.e4m3x2 h2, %2;\n\t"
-      "mov.b32 {lo, hi}, h2;\n\t"
-      "add.rn.f32.f16 %0, lo, %0;\n\t"
-      "add.rn.f32.f16 %1, hi, %1;\n\t}"
+// acc.x += the e4m3 values in bytes 0 and 2 of w, acc.y += bytes 1 and 3
+// (in that order; decoded exactly through f16, added with one rounding
+// each).
+__device__ __forceinline__ float2 add_e4m3x4_f32(float2 acc, uint32_t w) {
+  asm("{\n\t.reg .b32 h0, h1;\n\t.reg .b16 lo, hi, a0, a1, b0, b1;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h1, hi;\n\t"
+      "mov.b32 {a0, a1}, h0;\n\t"
+      "mov.b32 {b0, b1}, h1;\n\t"
+      "add.rn.f32.f16 %0, a0, %0;\n\t"
+      "add.rn.f32.f16 %1, a1, %1;\n\t"
+      "add.rn.f32.f16 %0, b0, %0;\n\t"
+      "add.rn.f32.f16 %1, b1, %1;\n\t}"
       : "+f"(acc.x), "+f"(acc.y)
-      : "h"(b));
+      : "r"(w));
   return acc;
 }
 
