@@ -8,26 +8,30 @@
 //     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D = rowsum(dO o O),
 //     dK = s dS^T Q,  dQ = s dS K.
 //
-// Three launches on the caller's stream, none with atomics, so every
-// output is bitwise reproducible:
+// Three launches, none with atomics, so every output is bitwise
+// reproducible:
 //   1. fa_bwd_pre_kernel   D = rowsum(dO o O) per query row (fp32) and the
 //                          saved logsumexp in log2 units, both padded to
 //                          whole blocks of 128 rows.
 //   2. fa_bwd_dkdv_kernel  one CTA per (head, block of 128 keys): K_j, V_j
 //                          stay in shared memory, dK_j and dV_j accumulate in
 //                          TMEM over the query blocks (4 products per block).
-//   3. fa_bwd_dq_kernel    one CTA per (head, block of 128 queries): Q_i, dO_i
-//                          stay in shared memory, dQ_i accumulates in TMEM
-//                          over the key blocks (3 products per block).
+//   3. fa_bwd_dq_kernel    one CTA per (head, block of 128 queries): Q_i and
+//                          dO_i stay in TMEM, dQ_i accumulates in TMEM over
+//                          the key blocks (3 products per block).
+// The dQ kernel reads only the inputs and the pre-kernel's statistics, so
+// it runs on a side stream next to the dK/dV kernel (forked from and joined
+// back to the caller's stream).  On short causal sequences both kernels
+// give each CTA a pair of mirror blocks of one head instead of one block.
 // Splitting dQ off costs two recomputed products per block pair but removes
 // the fp32 reduction of dQ across key blocks through L2, which otherwise
 // bounds the backward pass.
 //
 // Both main kernels: warp 0 TMA producer, warp 1 MMA issuer (one thread),
-// warp 2 TMEM owner; warps 4..11 own one row each (key row in dK/dV, query
-// row in dQ), two warps per row, each taking one half of the row's 128
-// columns; they work in two phases per block: P from the scores, then dS
-// from dP.
+// warp 2 TMEM owner; the row warps from warp 4 on own one row each (key row
+// in dK/dV, query row in dQ), two or four warps per row, each taking a
+// slice of the row's 128 columns; they work in two phases per block: P from
+// the scores, then dS from dP.
 
 #include "fa_internal.h"
 #include "ptx.cuh"
