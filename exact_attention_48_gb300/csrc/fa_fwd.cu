@@ -73,11 +73,21 @@ struct FwdLayout {
 constexpr int kThreads = 384;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 // Register split: 168 per thread at launch (384 x 168 fits the SM); the
-// control warpgroup gives back down to 104 and the two softmax warpgroups
-// take 200 each: 128*104 + 256*200 <= 384*168, and per SM sub-partition
-// (one warp of each warpgroup) 32*(104 + 2*200) <= 16384.
-constexpr uint32_t kRegsLaunch = 168, kRegsControl = 104, kRegsSoftmax = 200;
-static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+// control warpgroup gives registers back and the two softmax warpgroups take
+// them: at d = 128 104 and 200, at d = 64 152 and 176 (the MMA issuer's
+// unrolled d = 64 loops spill at 104; without the spills the d = 64 kernels
+// run 4 % faster, while the d = 128 ones are 1-2 % faster with the softmax
+// at 200).  128*control + 256*softmax <= 384*168, and per SM sub-partition
+// (one warp of each warpgroup) 32*(control + 2*softmax) <= 16384.
+constexpr uint32_t kRegsLaunch = 168;
+template <int D>
+constexpr uint32_t kRegsControl = (D == 64) ? 152 : 104;
+template <int D>
+constexpr uint32_t kRegsSoftmax = (D == 64) ? 176 : 200;
+static_assert(128 * kRegsControl<64> + 256 * kRegsSoftmax<64> <= kThreads * kRegsLaunch, "register split");
+static_assert(128 * kRegsControl<128> + 256 * kRegsSoftmax<128> <= kThreads * kRegsLaunch, "register split");
+static_assert(32 * (kRegsControl<64> + 2 * kRegsSoftmax<64>) <= 16384, "register split per sub-partition");
+static_assert(32 * (kRegsControl<128> + 2 * kRegsSoftmax<128>) <= 16384, "register split per sub-partition");
 
 // Columns of O in TMEM: d, plus 16 at d = 64 where the product also forms
 // the sum of the weights it applied.
@@ -377,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sV = smem + L::kOffV;
 
   if (warp >= kWarpProducer) {
-    regs_decrease<kRegsControl>();
+    regs_decrease<kRegsControl<D>>();
     if (warp == kWarpProducer && lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tm_q);
@@ -489,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(drain, 0);
     }
   } else {
-    regs_increase<kRegsSoftmax>();
+    regs_increase<kRegsSoftmax<D>>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
     SoftmaxArgs a;

@@ -41,7 +41,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kStale = 2;
 constexpr int kThreads = 384;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
-constexpr uint32_t kRegsLaunch = 168, kRegsControl = 104, kRegsSoftmax = 200;
+// Register split: 168 per thread at launch; the control warpgroup keeps 152
+// (at 104 its issue loops spilled) and the softmax warpgroups take 176:
+// 128*152 + 256*176 <= 384*168, and per SM sub-partition 32*(152 + 2*176)
+// <= 16384.
+constexpr uint32_t kRegsLaunch = 168, kRegsControl = 152, kRegsSoftmax = 176;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 
 struct F8Layout {
