@@ -442,15 +442,15 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
         float2 pf[kKvCols / 2];
         {
           uint32_t sva[kCh][32];
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tS + c0 + ch * 32, sva[ch]);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(sva[ch]);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) {
             const uint32_t(&sv)[32] = sva[ch];
             uint32_t pk[16];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const int qh = ch * 32 + e;  // query column within this thread's columns
               const float4 l4 = lse4[qh / 4];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
                                        make_float2(c, c), make_float2(-l4.z, -l4.w));
               float pr[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
               if (diag) {
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 4; ++u) pr[u] = (c0 + qh + u >= r) ? pr[u] : 0.0f;  // key r visible to query q iff r <= q
               }
               pf[qh / 2] = make_float2(pr[0], pr[1]);
@@ -485,15 +485,15 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
         tc_fence_after();
         {
           uint32_t dpa[kCh][32];
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) tmem_ld32(tDP + c0 + ch * 32, dpa[ch]);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) tmem_ld_wait(dpa[ch]);
-  #pragma unroll
+#pragma unroll
           for (int ch = 0; ch < kCh; ++ch) {
             const uint32_t(&dpv)[32] = dpa[ch];
             uint32_t dk[16];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const int qh = ch * 32 + e;
               const float4 d4 = del4[qh / 4];
@@ -861,21 +861,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < 2; ++ch) tmem_ld_wait(sva[ch]);
         tc_fence_before();
         warp_arrive(s_free);  // S is in registers: the next S may overwrite it
+        // (two copies, the mask flag fixed at compile time: the blocks that
+        // need no mask carry no masking instructions; with one body and a
+        // run-time test the causal kernel ran its ALU pipe at twice the
+        // non-causal one's rate)
+        auto form_p = [&](auto mask_tag) {
+          const bool masked = mask_tag;
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          const uint32_t(&sv)[32] = sva[ch];
+          for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t(&sv)[32] = sva[ch];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
-            float p0 = ex2(x.x), p1 = ex2(x.y);
-            if (diag || kmask) {  // key kc visible to query r iff kc <= r (causal) and kc < N
-              const int lim = diag ? min(r, klim) : klim;
-              p0 = (c0 + ch * 32 + e <= lim) ? p0 : 0.0f;
-              p1 = (c0 + ch * 32 + e + 1 <= lim) ? p1 : 0.0f;
+            for (int e = 0; e < 32; e += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc, nl);
+              float p0 = ex2(x.x), p1 = ex2(x.y);
+              if (masked) {  // key kc visible to query r iff kc <= r (causal) and kc < N
+                const int lim = diag ? min(r, klim) : klim;
+                p0 = (c0 + ch * 32 + e <= lim) ? p0 : 0.0f;
+                p1 = (c0 + ch * 32 + e + 1 <= lim) ? p1 : 0.0f;
+              }
+              pf[ch * 16 + e / 2] = make_float2(p0, p1);
             }
-            pf[ch * 16 + e / 2] = make_float2(p0, p1);
           }
-        }
+        };
+        if (diag || kmask)
+          form_p(MaskTag<true>{});
+        else
+          form_p(MaskTag<false>{});
 
         // Phase 2: dS = P o (dP - D) -> bf16 pairs over this half's own,
         // already read, dP columns (dQ(j-1) has read dS(j-1) from there: it

@@ -101,6 +101,11 @@ FP8_B2H16N8192D128 = Workload("fp8_b2h16n8192d128", 2, 16, 8192, 128, False, Fal
 # (bf16, contiguous [B, H, N, d] cache): HBM-bound, 2 GiB of cache per step.
 DECODE_B16H16NK16384D128 = Workload("decode_b16h16nk16384d128", 16, 16, 16384, 128, False, False, 1.0, 1007,
                                     "one query row per head against a 16384-key cache", layout="decode", nq=1)
+# The same cache with eight query rows per head (speculative or grouped
+# decoding): the products run on the tensor core.
+DECODE_B16H16NQ8NK16384D128 = Workload("decode_b16h16nq8nk16384d128", 16, 16, 16384, 128, False, False, 1.0, 1009,
+                                       "eight query rows per head against a 16384-key cache", layout="decode",
+                                       nq=8)
 
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
 HEADLINE = sweep(8192, 128, False)   # B=2, H=16, N=8192, d=128, non-causal
