@@ -815,14 +815,24 @@ def run_sweep(args):
                 mf, mb = statistics.median(tf), statistics.median(tb)
                 ftf = w.flops_fwd() / (mf * 1e-3) / 1e12
                 btf = w.flops_bwd() / (mb * 1e-3) / 1e12
-                # algorithmic HBM bytes of the forward: q, k, v read, o written, lse written
+                # algorithmic HBM bytes of the forward: q, k, v read, o written, lse written;
+                # of the backward: q, k, v, o, dO read, dq, dk, dv written, lse read
                 fbytes = 8.0 * w.B * w.H * w.N * w.d + 4.0 * w.B * w.H * w.N
+                bbytes = 16.0 * w.B * w.H * w.N * w.d + 4.0 * w.B * w.H * w.N
+                # roof of each pass: the tensor peak, or the HBM copy bandwidth
+                # times the pass's arithmetic intensity where that is lower
+                # (short or causal sequences)
+                froof = min(peaks["bf16_tflops"], w.flops_fwd() / fbytes * peaks["hbm_gbs"] / 1e3)
+                broof = min(peaks["bf16_tflops"], w.flops_bwd() / bbytes * peaks["hbm_gbs"] / 1e3)
                 print(json.dumps({"sweep": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "causal": causal,
                                   "fwd_ms": mf, "fwd_tflops": ftf, "fwd_frac_of_burst": ftf / peaks["bf16_tflops"],
                                   "fwd_frac_of_sustained": ftf / peaks["bf16_tflops_sustained"],
+                                  "fwd_roof_tflops": froof, "fwd_frac_of_roof": ftf / froof,
                                   "bwd_ms": mb, "bwd_tflops": btf, "bwd_frac_of_burst": btf / peaks["bf16_tflops"],
                                   "bwd_frac_of_sustained": btf / peaks["bf16_tflops_sustained"],
-                                  "fwd_hbm_gbs_algorithmic": fbytes / (mf * 1e-3) / 1e9, "peak_source": peak_src}),
+                                  "bwd_roof_tflops": broof, "bwd_frac_of_roof": btf / broof,
+                                  "fwd_hbm_gbs_algorithmic": fbytes / (mf * 1e-3) / 1e9,
+                                  "bwd_hbm_gbs_algorithmic": bbytes / (mb * 1e-3) / 1e9, "peak_source": peak_src}),
                       flush=True)
                 del q, k, v, do, o, lse, ws, dq, dk, dv
                 torch.cuda.empty_cache()
