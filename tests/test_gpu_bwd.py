@@ -83,13 +83,17 @@ def test_bwd_caller_workspace_and_reuse():
         assert torch.equal(a, b)
 
 
-def test_bwd_deterministic():
-    """dq, dk and dv are bitwise reproducible run to run."""
-    q, k, v, do = draw_shape(2, 4, 1000, 128, 13, 1.0, "cuda", torch.bfloat16)
-    o, lse = fa_fwd(q, k, v, False)
-    ref = fa_bwd(q, k, v, o, do, lse, False)
+@pytest.mark.parametrize("N,d,causal", [(1000, 128, False), (1000, 128, True), (1000, 64, True), (5000, 128, True)])
+def test_bwd_deterministic(N, d, causal):
+    """dq, dk and dv are bitwise reproducible run to run, with the causal
+    schedules too (N = 1000: mirror-block pairs in both kernels; N = 5000:
+    one block per CTA, heaviest first, the dQ kernel on its side stream
+    finishing in a different order from run to run)."""
+    q, k, v, do = draw_shape(2, 4, N, d, 13, 1.0, "cuda", torch.bfloat16)
+    o, lse = fa_fwd(q, k, v, causal)
+    ref = fa_bwd(q, k, v, o, do, lse, causal)
     for _ in range(3):
-        got = fa_bwd(q, k, v, o, do, lse, False)
+        got = fa_bwd(q, k, v, o, do, lse, causal)
         for a, b in zip(ref, got):
             assert torch.equal(a, b)
 
