@@ -18,8 +18,7 @@
 // cudaGetSymbolAddress (a host-side query: it enqueues nothing).  The
 // address is not cached: after cudaDeviceReset, or under another context on
 // the same device, the module is loaded again and the array may move.  The
-// first lookup in a process may load the module, so the first call should
-// come before any stream capture.
+// first lookup in a process may load the module.
 //
 // Every call uses the same array and leaves its last contents there.
 // Nothing in it has to start at zero: the first kernel of each call writes

@@ -286,9 +286,9 @@ FA_API fa_status_t fa_fwd_decode(const void *q, const int64_t *q_strides, const 
  * pass fa_bwd a workspace nor let it take one.
  *
  * Set-up and sharing: every call looks up the array's device address in
- * the current context (cudaGetSymbolAddress, a host-side query); the first
- * lookup in a process may load the module, so make the first call before
- * any stream capture.  All calls share the one array and it keeps the last
+ * the current context (cudaGetSymbolAddress, a host-side query; the first
+ * lookup in a process may load the library's device code).  All calls share
+ * the one array and it keeps the last
  * call's contents; nothing in it needs to start at zero.
  * Calls whose work overlaps on the GPU (other streams or host threads on
  * the same device) race on it, so the caller must order them.
