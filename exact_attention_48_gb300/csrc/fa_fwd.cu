@@ -7,7 +7,9 @@
 // pass, and a running row normalisation that corrects the partial output
 // whenever a larger score appears).  The grid spreads the query blocks of
 // every head over the SMs (page "FlashAttention-2 (DE)", "Technische
-// Architektur", section 2).
+// Architektur", section 2).  Short d = 64 sequences (non-causal, batched)
+// run a persistent grid instead: one CTA per SM takes such 256-row tiles in
+// turn and overlaps each tile's start with the previous tile's end.
 //
 // Roles inside the CTA (384 threads, three warpgroups):
 //   warps 0..3   softmax of tile 0, warps 4..7 softmax of tile 1: one query
@@ -49,21 +51,27 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+// QB: buffers of the two Q tiles (2 in the persistent kernel, which loads
+// the next 256 rows' Q while it still works on the current ones).
+template <int D, int QB>
 struct FwdLayout {
   static constexpr int kSlabs = D / 64;  // 128-byte column slabs of a bf16 row
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // K/V ring stages (three beside the persistent kernel's second Q buffer:
+  // measured as fast as four there)
+  static constexpr int kStages = (D == 64) ? (QB == 2 ? 3 : 4) : 2;
+  static constexpr int kQBufs = QB;
   static constexpr uint32_t kQTile = kBM * D * 2;
   static constexpr uint32_t kKVBytes = kBN * D * 2;
-  static constexpr uint32_t kOffQ = 0;  // two tiles
-  static constexpr uint32_t kOffK = kOffQ + 2 * kQTile;
+  static constexpr uint32_t kOffQ = 0;  // QB buffers of two tiles
+  static constexpr uint32_t kOffK = kOffQ + QB * 2 * kQTile;
   static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
   // d = 64: one 128-key slab of bf16 ones, the extra 16 columns of V in P V
   static constexpr uint32_t kOnesBytes = (D == 64) ? kBN * 128 : 0;
   static constexpr uint32_t kOffOnes = kOffV + kStages * kKVBytes;
   static constexpr uint32_t kOffBar = kOffOnes + kOnesBytes;
-  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2], pv_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+  // q_full[QB], q_empty[QB], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_ready[2],
+  // pv_done[2], drain
+  static constexpr int kNumBars = 2 * QB + 4 * kStages + 6 + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemRequest = kBytes + 1024;  // slack for 1024-byte alignment
@@ -77,17 +85,22 @@ constexpr int kWarpProducer = 8, kWarpMma = 9;
 // them: at d = 128 104 and 200, at d = 64 152 and 176 (the MMA issuer's
 // unrolled d = 64 loops spill at 104; without the spills the d = 64 kernels
 // run 4 % faster, while the d = 128 ones are 1-2 % faster with the softmax
-// at 200).  128*control + 256*softmax <= 384*168, and per SM sub-partition
-// (one warp of each warpgroup) 32*(control + 2*softmax) <= 16384.
+// at 200).  The persistent d = 64 kernel carries its tile loop's state
+// through the softmax and gives it 184 (136 for control): 2-3 % faster than
+// 152 and 176, where its softmax spilled.  128*control + 256*softmax <=
+// 384*168, and per SM sub-partition (one warp of each warpgroup)
+// 32*(control + 2*softmax) <= 16384.
 constexpr uint32_t kRegsLaunch = 168;
-template <int D>
-constexpr uint32_t kRegsControl = (D == 64) ? 152 : 104;
-template <int D>
-constexpr uint32_t kRegsSoftmax = (D == 64) ? 176 : 200;
-static_assert(128 * kRegsControl<64> + 256 * kRegsSoftmax<64> <= kThreads * kRegsLaunch, "register split");
-static_assert(128 * kRegsControl<128> + 256 * kRegsSoftmax<128> <= kThreads * kRegsLaunch, "register split");
-static_assert(32 * (kRegsControl<64> + 2 * kRegsSoftmax<64>) <= 16384, "register split per sub-partition");
-static_assert(32 * (kRegsControl<128> + 2 * kRegsSoftmax<128>) <= 16384, "register split per sub-partition");
+template <int D, bool PERSIST>
+constexpr uint32_t kRegsControl = (D == 64) ? (PERSIST ? 136 : 152) : 104;
+template <int D, bool PERSIST>
+constexpr uint32_t kRegsSoftmax = (D == 64) ? (PERSIST ? 184 : 176) : 200;
+template <int D, bool PERSIST>
+constexpr bool kRegSplitFits = 128 * kRegsControl<D, PERSIST> + 256 * kRegsSoftmax<D, PERSIST> <= kThreads * kRegsLaunch &&
+                               32 * (kRegsControl<D, PERSIST> + 2 * kRegsSoftmax<D, PERSIST>) <= 16384;
+static_assert(kRegSplitFits<64, false> && kRegSplitFits<64, true> && kRegSplitFits<128, false> &&
+                  kRegSplitFits<128, true>,
+              "register split");
 
 // Columns of O in TMEM: d, plus 16 at d = 64 where the product also forms
 // the sum of the weights it applied.
@@ -102,11 +115,13 @@ struct SoftmaxArgs {
   int grow0;        // first query row of the tile (within its sequence)
   int N;            // rows of this tile's sequence
   int row0;         // first row of the sequence on the tensors' row axis
+  int cb0;          // blocks this tile's barriers completed for earlier tiles (their phase base)
 };
 
-// Online softmax of one 128-row tile: one query row per thread.
+// Online softmax of one 128-row tile: one query row per thread.  Returns
+// false if a wait gave up.
 template <int D, bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdParams &p, const WaitCtl &ctl, int bh,
+__device__ __forceinline__ bool softmax_tile(const SoftmaxArgs &a, const FwdParams &p, const WaitCtl &ctl, int bh,
                                              int warp, int lane) {
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
@@ -130,7 +145,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
   // batched non-causal d = 128 kernel was 2 % faster with the one body.
   auto block = [&](const int j, auto mask) -> bool {
     const bool MASK = mask;
-    if (!__all_sync(0xffffffffu, mbar_wait(a.s_full, j & 1, ctl, kSiteSFull))) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(a.s_full, (a.cb0 + j) & 1, ctl, kSiteSFull))) return false;
     tc_fence_after();
     uint32_t s[4][32];
 #pragma unroll
@@ -215,7 +230,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     // complete; the wait only makes that explicit).  Rows that keep their
     // max leave O alone, and the next product simply accumulates into it.
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      if (!__all_sync(0xffffffffu, mbar_wait(a.pv_done, (j - 1) & 1, ctl, kSitePvDone))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(a.pv_done, (a.cb0 + j - 1) & 1, ctl, kSitePvDone))) return false;
       {
         tc_fence_after();
 #pragma unroll 1
@@ -266,7 +281,7 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
 
   // Epilogue: O / l in bf16 and the natural-log logsumexp.
   if (ok) {
-    ok = mbar_wait(a.pv_done, (a.n_kv - 1) & 1, ctl, kSitePvDone);
+    ok = mbar_wait(a.pv_done, (a.cb0 + a.n_kv - 1) & 1, ctl, kSitePvDone);
     ok = __all_sync(0xffffffffu, ok);
   }
   if (ok) {
@@ -300,20 +315,68 @@ __device__ __forceinline__ void softmax_tile(const SoftmaxArgs &a, const FwdPara
     if (store)
       p.lse[(bh / p.H) * p.lse_b + (bh % p.H) * p.lse_h + a.row0 + grow_row] = (m_run + log2f(l_run)) * kLn2;
   }
+  return ok;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+// One 256-row block of query rows of one (batch, head): what a CTA works on.
+struct FwdTile {
+  int bh, qb;      // (batch, head) index and 256-row block
+  int row0, N;     // the sequence's first row on the row axis, its length
+  int bh_h, bh_b;  // TMA coordinates of the head
+  int n0, n1;      // key blocks of its tiles 0 and 1 (n0 <= n1)
+  bool empty;      // packed mode: the block lies past its sequence's end
+};
+
+// Tile order.  Causal: the heaviest 256-row blocks (most key blocks) first,
+// across all heads.  Otherwise head-major so that CTAs running together
+// share the K/V of one head in L2.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ FwdTile fwd_tile(const FwdParams &p, int x) {
+  FwdTile t;
+  if (CAUSAL) {
+    t.qb = p.num_qblk - 1 - x / p.BH;
+    t.bh = x % p.BH;
+  } else {
+    t.bh = x / p.num_qblk;
+    t.qb = x % p.num_qblk;
+  }
+  const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, t.bh / p.H, p.N, p.T) : SeqRange{0, p.N};
+  t.empty = VARLEN && t.qb * 2 * kBM >= seq.len;
+  t.row0 = seq.start;
+  t.N = seq.len;
+  t.bh_h = t.bh % p.H;
+  t.bh_b = VARLEN ? 0 : t.bh / p.H;
+  const int nkv_all = (t.N + kBN - 1) / kBN;
+  t.n0 = CAUSAL ? min(2 * t.qb + 1, nkv_all) : nkv_all;
+  t.n1 = CAUSAL ? min(2 * t.qb + 2, nkv_all) : nkv_all;
+  return t;
+}
+
+// PERSIST: one CTA per SM walks the tiles x = blockIdx.x + r * gridDim.x
+// (r = 0, 1, ...); otherwise one CTA per tile.  The persistent kernel keeps
+// two Q buffers, so the next tile's Q arrives while the current tile is
+// worked on, and its first scores are formed while the softmax warps still
+// write the current tile's output: the load latency, pipeline fill and
+// epilogue that a CTA of its own pays per tile overlap the neighbouring
+// tiles' work.  The K/V ring and every barrier's phase run on across tiles.
+template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdLayout<D>;
+  static_assert(!(PERSIST && VARLEN), "the packed mode launches one CTA per tile");
+  constexpr int QB = PERSIST ? 2 : 1;
+  using L = FwdLayout<D, QB>;
   constexpr int S = L::kStages;
+  // tiles a CTA takes at most (the persistent loop ends on the tile count)
+  constexpr int kRounds = PERSIST ? 0x7fffffff : 1;
+  const int num_tiles = p.BH * p.num_qblk;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-  uint64_t *q_full = bars;
-  uint64_t *k_full = bars + 1;
+  uint64_t *q_full = bars;          // [QB]
+  uint64_t *q_empty = q_full + QB;  // [QB]
+  uint64_t *k_full = q_empty + QB;
   uint64_t *k_empty = k_full + S;
   uint64_t *v_full = k_empty + S;
   uint64_t *v_empty = v_full + S;
@@ -328,30 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Tile order.  Causal: the heaviest 256-row blocks (most key blocks)
-  // first, across all heads.  Otherwise head-major so that CTAs running
-  // together share the K/V of one head in L2.
-  int bh, qb;
-  if (CAUSAL) {
-    qb = p.num_qblk - 1 - static_cast<int>(blockIdx.x) / p.BH;
-    bh = static_cast<int>(blockIdx.x) % p.BH;
-  } else {
-    bh = static_cast<int>(blockIdx.x) / p.num_qblk;
-    qb = static_cast<int>(blockIdx.x) % p.num_qblk;
+  // A CTA of its own takes its tile here (and has no work if the tile lies
+  // past its sequence's end, packed mode); persistent CTAs take theirs in
+  // each role's tile loop.
+  FwdTile own{};
+  if constexpr (!PERSIST) {
+    own = fwd_tile<CAUSAL, VARLEN>(p, static_cast<int>(blockIdx.x));
+    if (own.empty) return;
   }
-  // The tile's sequence; a tile past its end (packed mode) has no work.
-  const SeqRange seq = VARLEN ? seq_range(p.cu_seqlens, bh / p.H, p.N, p.T) : SeqRange{0, p.N};
-  if (VARLEN && qb * 2 * kBM >= seq.len) return;
-  const int row0 = seq.start;
-  const int bh_h = bh % p.H, bh_b = VARLEN ? 0 : bh / p.H;  // TMA coordinates of the head
-  const int N = seq.len;
-  const int nkv_all = (N + kBN - 1) / kBN;
-  const int n0 = CAUSAL ? min(2 * qb + 1, nkv_all) : nkv_all;  // key blocks of tile 0
-  const int n1 = CAUSAL ? min(2 * qb + 2, nkv_all) : nkv_all;  // key blocks of tile 1 (>= n0)
-  const int n_kv = n1;
+  auto tile_at = [&](int x) -> FwdTile {
+    if constexpr (PERSIST)
+      return fwd_tile<CAUSAL, VARLEN>(p, x);
+    else
+      return own;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int b = 0; b < QB; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -387,133 +446,179 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sV = smem + L::kOffV;
 
   if (warp >= kWarpProducer) {
-    regs_decrease<kRegsControl<D>>();
+    regs_decrease<kRegsControl<D, PERSIST>>();
     if (warp == kWarpProducer && lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
+      int g = 0;  // K/V blocks loaded so far, over all tiles (ring position)
+      int q_issued = 0, k_issued = 0, v_issued = 0;
+      bool run = true;
+      for (int r = 0; run && r < kRounds; ++r) {
+        const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+        if (PERSIST && x >= num_tiles) break;
+        const FwdTile tl = tile_at(x);
+        const int qbuf = r % QB;
+        if (!mbar_wait(&q_empty[qbuf], ((r / QB) & 1) ^ 1, ctl, kSiteQEmpty)) break;
+        mbar_arrive_expect_tx(&q_full[qbuf], 2 * L::kQTile);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sQ + t * L::kQTile + s * kBM * 128, &tm_q, q_full, s * 64, row0 + qb * 2 * kBM + t * kBM, bh_h,
-                      bh_b);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        const uint32_t ph = (j / S) & 1;
-        if (!mbar_wait(&k_empty[st], ph ^ 1, ctl, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
+          for (int s = 0; s < L::kSlabs; ++s)
+            tma_load_4d(sQ + (qbuf * 2 + t) * L::kQTile + s * kBM * 128, &tm_q, &q_full[qbuf], s * 64,
+                        tl.row0 + tl.qb * 2 * kBM + t * kBM, tl.bh_h, tl.bh_b);
+        q_issued = r + 1;
+        for (int j = 0; j < tl.n1; ++j, ++g) {
+          const int st = g % S;
+          const uint32_t ph = (g / S) & 1;
+          if (!mbar_wait(&k_empty[st], ph ^ 1, ctl, kSiteKEmpty)) {
+            run = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBN, bh_h, bh_b);
-        k_issued = j + 1;
+          for (int s = 0; s < L::kSlabs; ++s)
+            tma_load_4d(sK + st * L::kKVBytes + s * kBN * 128, &tm_k, &k_full[st], s * 64, tl.row0 + j * kBN,
+                        tl.bh_h, tl.bh_b);
+          k_issued = g + 1;
 #ifdef FA_TEST_SKIP_FIRST_V_LOAD
-        // Test builds only: the first V block is never loaded, so the MMA
-        // thread's wait for it runs out and the bounded-wait path is taken.
-        if (j == 0) continue;
+          // Test builds only: the first V block is never loaded, so the MMA
+          // thread's wait for it runs out and the bounded-wait path is taken.
+          if (g == 0) continue;
 #endif
-        if (!mbar_wait(&v_empty[st], ph ^ 1, ctl, kSiteVEmpty)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
+          if (!mbar_wait(&v_empty[st], ph ^ 1, ctl, kSiteVEmpty)) {
+            run = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
 #pragma unroll
-        for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBN, bh_h, bh_b);
-        v_issued = j + 1;
+          for (int s = 0; s < L::kSlabs; ++s)
+            tma_load_4d(sV + st * L::kKVBytes + s * kBN * 128, &tm_v, &v_full[st], s * 64, tl.row0 + j * kBN,
+                        tl.bh_h, tl.bh_b);
+          v_issued = g + 1;
+        }
       }
       // Every copy issued lands before this thread leaves, whatever the
       // other roles do: after a timeout elsewhere in the CTA nobody else
       // waits for them.  (Bounded waits; in a normal run they are done.)
-      mbar_drain(q_full, 0);
-      for (int j = (k_issued > S ? k_issued - S : 0); j < k_issued; ++j) mbar_drain(&k_full[j % S], (j / S) & 1);
-      for (int j = (v_issued > S ? v_issued - S : 0); j < v_issued; ++j) mbar_drain(&v_full[j % S], (j / S) & 1);
+      for (int i = (q_issued > QB ? q_issued - QB : 0); i < q_issued; ++i) mbar_drain(&q_full[i % QB], (i / QB) & 1);
+      for (int i = (k_issued > S ? k_issued - S : 0); i < k_issued; ++i) mbar_drain(&k_full[i % S], (i / S) & 1);
+      for (int i = (v_issued > S ? v_issued - S : 0); i < v_issued; ++i) mbar_drain(&v_full[i % S], (i / S) & 1);
     } else if (warp == kWarpMma && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16(kBM, kOW<D>, false, true);
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
       // TMEM columns of tile t: S at t*128, O at 256 + t*kOW<D>
+      int g = 0;           // ring position of the current tile's first K/V block
+      int c0 = 0, c1 = 0;  // blocks tiles 0 and 1 finished in earlier tiles (barrier phases)
+      bool ok = true;
+      for (int r = 0; ok && r < kRounds; ++r) {
+        const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+        if (PERSIST && x >= num_tiles) break;
+        const FwdTile tl = tile_at(x);
+        const int n0 = tl.n0, n_kv = tl.n1;
+        const int qbuf = r % QB;
 
-      // Descriptors: the Q tiles once, K/V per stage; every MMA adds a
-      // compile-time step offset (the issue loops are unrolled).
-      const uint64_t dQ0 = sdesc_sw128(aQ, 16, 1024), dQ1 = sdesc_sw128(aQ + L::kQTile, 16, 1024);
+        // Descriptors: the Q tiles once, K/V per stage; every MMA adds a
+        // compile-time step offset (the issue loops are unrolled).
+        const uint64_t dQ0 = sdesc_sw128(aQ + qbuf * 2 * L::kQTile, 16, 1024),
+                       dQ1 = sdesc_sw128(aQ + (qbuf * 2 + 1) * L::kQTile, 16, 1024);
 
-      // S_t = Q_t K_j^T (both operands K-major over d)
-      auto issue_s = [&](int t, int j) {
-        const uint64_t bq = t ? dQ1 : dQ0, bk = sdesc_sw128(aK + (j % S) * L::kKVBytes, 16, 1024);
+        // S_t = Q_t K_j^T (both operands K-major over d)
+        auto issue_s = [&](int t, int j) {
+          const uint64_t bq = t ? dQ1 : dQ0, bk = sdesc_sw128(aK + ((g + j) % S) * L::kKVBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + t * 128, desc_add(bq, kmajor_step(kk, kBM)), desc_add(bk, kmajor_step(kk, kBN)), kIdescS,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(&s_full[t]);
-      };
-      // O_t += P_t V_j; P_t sits (bf16, two per column) over S_t in TMEM and
-      // V_j is [key][d]: MN-major for this product (d contiguous); 16 keys =
-      // two 8-row groups of 1024 bytes, d slabs 128*128 bytes apart.
-      auto issue_pv = [&](int t, int j) -> bool {
-        if (!mbar_wait(&p_ready[t], j & 1, ctl, kSitePReady)) return false;
-        tc_fence_after();
-        const uint32_t aVj = aV + (j % S) * L::kKVBytes;
-        // (d = 64: the slab after V's one column slab is the ones slab)
-        const uint64_t bv = sdesc_sw128(aVj, D == 64 ? smem_addr(smem + L::kOffOnes) - aVj : kBN * 128, 1024);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + t * 128, desc_add(bq, kmajor_step(kk, kBM)), desc_add(bk, kmajor_step(kk, kBN)), kIdescS,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(&s_full[t]);
+        };
+        // O_t += P_t V_j; P_t sits (bf16, two per column) over S_t in TMEM
+        // and V_j is [key][d]: MN-major for this product (d contiguous); 16
+        // keys = two 8-row groups of 1024 bytes, d slabs 128*128 bytes apart.
+        // The tile's first product overwrites O: the softmax warps have
+        // read the previous tile's O before they release this P.
+        auto issue_pv = [&](int t, int j) -> bool {
+          if (!mbar_wait(&p_ready[t], ((t ? c1 : c0) + j) & 1, ctl, kSitePReady)) return false;
+          tc_fence_after();
+          const uint32_t aVj = aV + ((g + j) % S) * L::kKVBytes;
+          // (d = 64: the slab after V's one column slab is the ones slab)
+          const uint64_t bv = sdesc_sw128(aVj, D == 64 ? smem_addr(smem + L::kOffOnes) - aVj : kBN * 128, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + t * kOW<D>, tmem + t * 128 + kk * 8, desc_add(bv, mnmajor_step(kk)), kIdescO,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&pv_done[t]);
-        return true;
-      };
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + 256 + t * kOW<D>, tmem + t * 128 + kk * 8, desc_add(bv, mnmajor_step(kk)), kIdescO,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&pv_done[t]);
+          return true;
+        };
+        auto kv_wait = [&](uint64_t *full, int j, int site) {
+          return mbar_wait(&full[(g + j) % S], ((g + j) / S) & 1, ctl, site);
+        };
 
-      bool ok = mbar_wait(q_full, 0, ctl, kSiteQFull) && mbar_wait(&k_full[0], 0, ctl, kSiteKFull);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc_commit(&k_empty[0]);
-      }
-      for (int j = 1; ok && j < n_kv; ++j) {
-        const int pj = j - 1;
-        if (!(ok = mbar_wait(&v_full[pj % S], (pj / S) & 1, ctl, kSiteVFull))) break;
-        tc_fence_after();
-        if (pj < n0 && !(ok = issue_pv(0, pj))) break;
-        if (!(ok = mbar_wait(&k_full[j % S], (j / S) & 1, ctl, kSiteKFull))) break;
-        tc_fence_after();
-        if (j < n0) issue_s(0, j);
-        if (!(ok = issue_pv(1, pj))) break;
-        tc_commit(&v_empty[pj % S]);
-        issue_s(1, j);
-        tc_commit(&k_empty[j % S]);
-      }
-      if (ok) {
-        const int pj = n_kv - 1;
-        ok = mbar_wait(&v_full[pj % S], (pj / S) & 1, ctl, kSiteVFull);
+        ok = mbar_wait(&q_full[qbuf], (r / QB) & 1, ctl, kSiteQFull) && kv_wait(k_full, 0, kSiteKFull);
         if (ok) {
           tc_fence_after();
-          if (pj < n0) ok = issue_pv(0, pj);
-          if (ok) ok = issue_pv(1, pj);
-          tc_commit(&v_empty[pj % S]);
+          issue_s(0, 0);
+          issue_s(1, 0);
+          tc_commit(&k_empty[g % S]);
         }
+        for (int j = 1; ok && j < n_kv; ++j) {
+          const int pj = j - 1;
+          if (!(ok = kv_wait(v_full, pj, kSiteVFull))) break;
+          tc_fence_after();
+          if (pj < n0 && !(ok = issue_pv(0, pj))) break;
+          if (!(ok = kv_wait(k_full, j, kSiteKFull))) break;
+          tc_fence_after();
+          if (j < n0) issue_s(0, j);
+          if (!(ok = issue_pv(1, pj))) break;
+          tc_commit(&v_empty[(g + pj) % S]);
+          issue_s(1, j);
+          tc_commit(&k_empty[(g + j) % S]);
+        }
+        if (ok) {
+          tc_commit(&q_empty[qbuf]);  // every product that reads this Q buffer is issued
+          const int pj = n_kv - 1;
+          ok = kv_wait(v_full, pj, kSiteVFull);
+          if (ok) {
+            tc_fence_after();
+            if (pj < n0) ok = issue_pv(0, pj);
+            if (ok) ok = issue_pv(1, pj);
+            tc_commit(&v_empty[(g + pj) % S]);
+          }
+        }
+        g += n_kv;
+        c0 += n0;
+        c1 += n_kv;
       }
       tc_commit(drain);
       mbar_drain(drain, 0);
     }
   } else {
-    regs_increase<kRegsSoftmax<D>>();
+    regs_increase<kRegsSoftmax<D, PERSIST>>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
-    SoftmaxArgs a;
-    a.s_full = &s_full[t];
-    a.p_ready = &p_ready[t];
-    a.pv_done = &pv_done[t];
-    a.tS = tmem + t * 128;
-    a.tO = tmem + 256 + t * kOW<D>;
-    a.n_kv = t ? n1 : n0;
-    a.diag = CAUSAL ? 2 * qb + t : -1;
-    a.grow0 = qb * 2 * kBM + t * kBM;
-    a.N = N;
-    a.row0 = row0;
-    softmax_tile<D, CAUSAL, VARLEN>(a, p, ctl, bh, warp, lane);
+    int cb = 0;  // blocks this tile's barriers completed in earlier tiles
+    for (int r = 0; r < kRounds; ++r) {
+      const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+      if (PERSIST && x >= num_tiles) break;
+      const FwdTile tl = tile_at(x);
+      SoftmaxArgs a;
+      a.s_full = &s_full[t];
+      a.p_ready = &p_ready[t];
+      a.pv_done = &pv_done[t];
+      a.tS = tmem + t * 128;
+      a.tO = tmem + 256 + t * kOW<D>;
+      a.n_kv = t ? tl.n1 : tl.n0;
+      a.diag = CAUSAL ? 2 * tl.qb + t : -1;
+      a.grow0 = tl.qb * 2 * kBM + t * kBM;
+      a.N = tl.N;
+      a.row0 = tl.row0;
+      a.cb0 = cb;
+      if (!softmax_tile<D, CAUSAL, VARLEN>(a, p, ctl, tl.bh, warp, lane)) break;
+      cb += a.n_kv;
+    }
   }
 
   tc_fence_before();
@@ -524,14 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const FwdParams &p,
                          cudaStream_t stream) {
-  using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
+  using L = FwdLayout<D, PERSIST ? 2 : 1>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, PERSIST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_qblk);
+  const unsigned tiles = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.num_qblk);
+  const unsigned ctas = static_cast<unsigned>(p.persist_ctas);
+  const unsigned grid = (PERSIST && ctas < tiles) ? ctas : tiles;
   kern<<<grid, kThreads, L::kSmemRequest, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -544,11 +651,13 @@ cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensor
   // carry none of its per-tile work)
   const bool v = p.cu_seqlens != nullptr;
   if (d == 64) {
-    if (causal) return v ? launch_fwd_t<64, true, true>(tq, tk, tv, p, stream) : launch_fwd_t<64, true, false>(tq, tk, tv, p, stream);
-    return v ? launch_fwd_t<64, false, true>(tq, tk, tv, p, stream) : launch_fwd_t<64, false, false>(tq, tk, tv, p, stream);
+    if (causal) return v ? launch_fwd_t<64, true, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<64, true, false, false>(tq, tk, tv, p, stream);
+    if (v) return launch_fwd_t<64, false, true, false>(tq, tk, tv, p, stream);
+    return p.persist_ctas > 0 ? launch_fwd_t<64, false, false, true>(tq, tk, tv, p, stream)
+                              : launch_fwd_t<64, false, false, false>(tq, tk, tv, p, stream);
   }
-  if (causal) return v ? launch_fwd_t<128, true, true>(tq, tk, tv, p, stream) : launch_fwd_t<128, true, false>(tq, tk, tv, p, stream);
-  return v ? launch_fwd_t<128, false, true>(tq, tk, tv, p, stream) : launch_fwd_t<128, false, false>(tq, tk, tv, p, stream);
+  if (causal) return v ? launch_fwd_t<128, true, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<128, true, false, false>(tq, tk, tv, p, stream);
+  return v ? launch_fwd_t<128, false, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<128, false, false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace fa

@@ -29,6 +29,7 @@ enum WaitSite : int {
   kSiteKvFull,
   kSiteMmaDone,
   kSiteKvEmpty,
+  kSiteQEmpty,
 };
 
 // Element strides of a [B, H, N, d] bf16 tensor whose d elements are
@@ -72,6 +73,7 @@ struct FwdParams {
   int N;
   int BH;
   int num_qblk;       // ceil(N / 256): one CTA per 256 query rows
+  int persist_ctas;   // > 0: persistent launch of this many CTAs walking the 256-row tiles
   float scale_log2;   // scale * log2(e)
   int neg;            // scale < 0
 };

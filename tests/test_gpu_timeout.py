@@ -40,8 +40,11 @@ def _stall_lib():
     return lib
 
 
-def test_timeout_is_reported_and_the_context_survives():
-    B, H, N, d = 1, 1, 256, 128       # one CTA, two key blocks
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 256, 128), (1, 160, 256, 64)])
+def test_timeout_is_reported_and_the_context_survives(B, H, N, d):
+    """(1, 1, 256, 128): one CTA, two key blocks.  (1, 160, 256, 64): more
+    tiles than SMs, so persistent CTAs that would each walk one or two
+    tiles; every one gives up in its first tile and takes no other."""
     scale = 1 / math.sqrt(d)
     q, k, v, _ = draw_shape(B, H, N, d, 61, 1.0, "cuda", torch.bfloat16)
     lib = _stall_lib()
