@@ -178,8 +178,19 @@ constexpr long long kMaxGridX = 2147483647LL;  // largest x extent of a launch g
 // 128: dK/dV +2..+11 % up to N = 4096 and -1..-3 % above; dQ +2..+7 % up to
 // N = 1024, even at 2048, -2..-6 % above.
 constexpr int kPairMaxBlocksKv = 32, kPairMaxBlocksQ = 16;
-// Longest sequence, in 256-row tiles, for the persistent d = 64 forward.
-constexpr int kPersistMaxQblk = 32;
+// Longest sequence, in 256-row tiles, for which the batched forward runs
+// persistent CTAs.  Measured against one CTA per tile (forward only, L2
+// flushed, B*N = 16384, H = 16):
+//   d = 64:   +27 % at N = 512, +15 % at 1024, +7 % at 2048, +2.5 % at 4096,
+//             +0.3 % at 8192, -0.7 % at 16384; causal +8.5 % at 512, +3 %
+//             at 2048, -1 % at 8192;
+//   d = 128:  +14 % at 512, +8 % at 1024, +2 % at 2048, -2 % at 4096, -5 %
+//             at 8192; causal +12 %, +9 %, +5 %, +3 % (N = 4096; +3.7 % at
+//             B4 H32), 0 % at 8192, -3 % at 16384.
+int persist_max_qblk(int d, bool causal) {
+  if (d == 64) return causal ? 16 : 32;
+  return causal ? 16 : 8;
+}
 
 // Host-side checks shared by both passes; no CUDA call happens before them.
 fa_status_t check_common(int B, int H, int N, int d, int causal, float scale) {
@@ -294,12 +305,9 @@ fa_status_t fwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   p.N = N;
   p.BH = B * H;
   p.num_qblk = (N + 255) / 256;
-  // The d = 64 batched non-causal forward runs persistent CTAs (one per SM)
-  // when there are more 256-row tiles than SMs and sequences of at most
-  // kPersistMaxQblk tiles (N <= 8192): measured (B*N = 16384, H = 16)
-  // +27 % at N = 512, +15 % at 1024, +7 % at 2048, +2.5 % at 4096, +0.3 % at
-  // 8192 and -0.7 % at 16384 against one CTA per tile.
-  if (d == 64 && !causal && !ax.cu && p.num_qblk <= kPersistMaxQblk) {
+  // The batched forward of short sequences runs persistent CTAs (one per
+  // SM) when there are more 256-row tiles than SMs.
+  if (!ax.cu && p.num_qblk <= persist_max_qblk(d, causal != 0)) {
     const int sms = sm_count();
     if (sms > 0 && static_cast<long long>(p.BH) * p.num_qblk > sms) p.persist_ctas = sms;
   }

@@ -7,9 +7,9 @@
 // pass, and a running row normalisation that corrects the partial output
 // whenever a larger score appears).  The grid spreads the query blocks of
 // every head over the SMs (page "FlashAttention-2 (DE)", "Technische
-// Architektur", section 2).  Short d = 64 sequences (non-causal, batched)
-// run a persistent grid instead: one CTA per SM takes such 256-row tiles in
-// turn and overlaps each tile's start with the previous tile's end.
+// Architektur", section 2).  Short batched sequences run a persistent grid
+// instead: one CTA per SM takes such 256-row tiles in turn and overlaps each
+// tile's start with the previous tile's end.
 //
 // Roles inside the CTA (384 threads, three warpgroups):
 //   warps 0..3   softmax of tile 0, warps 4..7 softmax of tile 1: one query
@@ -51,8 +51,9 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kTmemCols = 512;
 
-// QB: buffers of the two Q tiles (2 in the persistent kernel, which loads
-// the next 256 rows' Q while it still works on the current ones).
+// QB: buffers of the two Q tiles (2 in the persistent d = 64 kernel, which
+// loads the next 256 rows' Q while it still works on the current ones; at
+// d = 128 a second 64 KB buffer does not fit beside the K/V ring).
 template <int D, int QB>
 struct FwdLayout {
   static constexpr int kSlabs = D / 64;  // 128-byte column slabs of a bf16 row
@@ -101,6 +102,10 @@ constexpr bool kRegSplitFits = 128 * kRegsControl<D, PERSIST> + 256 * kRegsSoftm
 static_assert(kRegSplitFits<64, false> && kRegSplitFits<64, true> && kRegSplitFits<128, false> &&
                   kRegSplitFits<128, true>,
               "register split");
+
+// Buffers of a CTA's two Q tiles (see FwdLayout).
+template <int D, bool PERSIST>
+constexpr int kQBufs = (PERSIST && D == 64) ? 2 : 1;
 
 // Columns of O in TMEM: d, plus 16 at d = 64 where the product also forms
 // the sum of the weights it applied.
@@ -352,19 +357,22 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams &p, int x) {
   return t;
 }
 
-// PERSIST: one CTA per SM walks the tiles x = blockIdx.x + r * gridDim.x
-// (r = 0, 1, ...); otherwise one CTA per tile.  The persistent kernel keeps
-// two Q buffers, so the next tile's Q arrives while the current tile is
-// worked on, and its first scores are formed while the softmax warps still
-// write the current tile's output: the load latency, pipeline fill and
-// epilogue that a CTA of its own pays per tile overlap the neighbouring
-// tiles' work.  The K/V ring and every barrier's phase run on across tiles.
+// PERSIST: one CTA per SM walks the tiles (round r = 0, 1, ... takes tile
+// r * gridDim.x + blockIdx.x, mirrored in odd rounds when causal);
+// otherwise one CTA per tile.  At d = 64 the persistent kernel keeps two Q
+// buffers, so the next tile's Q arrives while the current tile is worked
+// on, and its first scores are formed while the softmax warps still write
+// the current tile's output: the load latency, pipeline fill and epilogue
+// that a CTA of its own pays per tile overlap the neighbouring tiles' work.
+// At d = 128 (one Q buffer) the next tile's Q loads once the current tile's
+// last scores are complete, while its last P V products and its epilogue
+// run.  The K/V ring and every barrier's phase run on across tiles.
 template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   static_assert(!(PERSIST && VARLEN), "the packed mode launches one CTA per tile");
-  constexpr int QB = PERSIST ? 2 : 1;
+  constexpr int QB = kQBufs<D, PERSIST>;
   using L = FwdLayout<D, QB>;
   constexpr int S = L::kStages;
   // tiles a CTA takes at most (the persistent loop ends on the tile count)
@@ -399,6 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     own = fwd_tile<CAUSAL, VARLEN>(p, static_cast<int>(blockIdx.x));
     if (own.empty) return;
   }
+  // Persistent CTAs take tile r * G + c in round r (G CTAs, c = blockIdx);
+  // causal tiles come heaviest first, and odd rounds run c backwards so that
+  // each CTA's heavy and light tiles even out.
+  auto tile_index = [&](int r) -> int {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return r * G + ((CAUSAL && (r & 1)) ? G - 1 - c : c);
+  };
   auto tile_at = [&](int x) -> FwdTile {
     if constexpr (PERSIST)
       return fwd_tile<CAUSAL, VARLEN>(p, x);
@@ -456,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued = 0, k_issued = 0, v_issued = 0;
       bool run = true;
       for (int r = 0; run && r < kRounds; ++r) {
-        const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+        const int x = tile_index(r);
         if (PERSIST && x >= num_tiles) break;
         const FwdTile tl = tile_at(x);
         const int qbuf = r % QB;
@@ -515,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c0 = 0, c1 = 0;  // blocks tiles 0 and 1 finished in earlier tiles (barrier phases)
       bool ok = true;
       for (int r = 0; ok && r < kRounds; ++r) {
-        const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+        const int x = tile_index(r);
         if (PERSIST && x >= num_tiles) break;
         const FwdTile tl = tile_at(x);
         const int n0 = tl.n0, n_kv = tl.n1;
@@ -601,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     int cb = 0;  // blocks this tile's barriers completed in earlier tiles
     for (int r = 0; r < kRounds; ++r) {
-      const int x = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+      const int x = tile_index(r);
       if (PERSIST && x >= num_tiles) break;
       const FwdTile tl = tile_at(x);
       SoftmaxArgs a;
@@ -632,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const FwdParams &p,
                          cudaStream_t stream) {
-  using L = FwdLayout<D, PERSIST ? 2 : 1>;
+  using L = FwdLayout<D, kQBufs<D, PERSIST>>;
   auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, PERSIST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return e;
@@ -647,17 +662,23 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, cudaStream_t stream) {
-  // (the packed-sequence mode is a template parameter: the batched kernels
-  // carry none of its per-tile work)
-  const bool v = p.cu_seqlens != nullptr;
+  // (the packed-sequence mode and the persistent grid are template
+  // parameters: the other kernels carry none of their per-tile work)
+  const bool v = p.cu_seqlens != nullptr, pers = p.persist_ctas > 0 && !v;
   if (d == 64) {
-    if (causal) return v ? launch_fwd_t<64, true, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<64, true, false, false>(tq, tk, tv, p, stream);
-    if (v) return launch_fwd_t<64, false, true, false>(tq, tk, tv, p, stream);
-    return p.persist_ctas > 0 ? launch_fwd_t<64, false, false, true>(tq, tk, tv, p, stream)
-                              : launch_fwd_t<64, false, false, false>(tq, tk, tv, p, stream);
+    if (v) return causal ? launch_fwd_t<64, true, true, false>(tq, tk, tv, p, stream)
+                         : launch_fwd_t<64, false, true, false>(tq, tk, tv, p, stream);
+    if (causal) return pers ? launch_fwd_t<64, true, false, true>(tq, tk, tv, p, stream)
+                            : launch_fwd_t<64, true, false, false>(tq, tk, tv, p, stream);
+    return pers ? launch_fwd_t<64, false, false, true>(tq, tk, tv, p, stream)
+                : launch_fwd_t<64, false, false, false>(tq, tk, tv, p, stream);
   }
-  if (causal) return v ? launch_fwd_t<128, true, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<128, true, false, false>(tq, tk, tv, p, stream);
-  return v ? launch_fwd_t<128, false, true, false>(tq, tk, tv, p, stream) : launch_fwd_t<128, false, false, false>(tq, tk, tv, p, stream);
+  if (v) return causal ? launch_fwd_t<128, true, true, false>(tq, tk, tv, p, stream)
+                       : launch_fwd_t<128, false, true, false>(tq, tk, tv, p, stream);
+  if (causal) return pers ? launch_fwd_t<128, true, false, true>(tq, tk, tv, p, stream)
+                          : launch_fwd_t<128, true, false, false>(tq, tk, tv, p, stream);
+  return pers ? launch_fwd_t<128, false, false, true>(tq, tk, tv, p, stream)
+              : launch_fwd_t<128, false, false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace fa

@@ -109,29 +109,31 @@ def test_fwd_constant_v_and_zero_q():
     assert torch.allclose(lse.double(), torch.full_like(lse.double(), math.log(N)), atol=1e-3)
 
 
+@pytest.mark.parametrize("d,causal", [(64, False), (64, True), (128, False), (128, True)])
 @pytest.mark.parametrize("B,H,N", [(3, 40, 1000), (1, 200, 1), (1, 160, 300), (2, 100, 129)])
-def test_fwd_persistent_same_bits_as_one_cta_per_tile(B, H, N):
-    """With more 256-row tiles than SMs, the d = 64 non-causal forward runs
-    one persistent CTA per SM that walks several tiles (two Q buffers, the
-    K/V ring and every barrier's phase carried from tile to tile); the
-    packed-sequence call runs one CTA per tile.  A tile's arithmetic is the
-    same either way, so the bits must be.  The shapes give ragged last tiles,
-    single-key heads and tile counts that are not multiples of the SM count
-    (some CTAs take one tile more than others); heads of the first and the
-    last round are also checked against the oracle."""
-    d = 64
+def test_fwd_persistent_same_bits_as_one_cta_per_tile(B, H, N, d, causal):
+    """With more 256-row tiles than SMs, the batched forward of short
+    sequences runs one persistent CTA per SM that walks several tiles (more
+    Q slots, the K/V ring and every barrier's phase carried from tile to
+    tile); the packed-sequence call runs one CTA per tile.  A tile's
+    arithmetic is the same either way, so the bits must be.  The shapes give
+    ragged last tiles, single-key heads and tile counts that are not
+    multiples of the SM count (some CTAs take one tile more than others);
+    heads of the first and the last round are also checked against the
+    oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert B * H * ((N + 255) // 256) > sms
     q, k, v, _ = draw_shape(B, H, N, d, 500 + N, 1.0, "cuda", torch.bfloat16, with_dout=False)
-    o, lse = fa_fwd(q, k, v, False)
+    o, lse = fa_fwd(q, k, v, causal)
     qp, kp, vp = (t.transpose(1, 2).reshape(B * N, H, d).contiguous() for t in (q, k, v))
     cu = torch.arange(0, B * N + 1, N, dtype=torch.int32, device="cuda")
-    o_p, lse_p = fa_fwd_varlen(qp, kp, vp, cu, N, False)
+    o_p, lse_p = fa_fwd_varlen(qp, kp, vp, cu, N, causal)
     assert fa_device_status() == 0
     assert torch.equal(o_p.reshape(B, N, H, d).transpose(1, 2), o)
     assert torch.equal(lse_p.reshape(H, B, N).permute(1, 0, 2), lse)
     scale = 1.0 / math.sqrt(d)
     for b, h in {(0, 0), (B - 1, H - 1), (B // 2, H // 2)}:
-        o_ref, lse_ref = oracle.fwd(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), False, scale)
-        check_o(o[b, h], o_ref, f"persistent B={B} H={H} N={N} head ({b}, {h})")
-        check_lse(lse[b, h], lse_ref, f"persistent B={B} H={H} N={N} head ({b}, {h})")
+        o_ref, lse_ref = oracle.fwd(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), causal, scale)
+        what = f"persistent B={B} H={H} N={N} d={d} causal={causal} head ({b}, {h})"
+        check_o(o[b, h], o_ref, what)
+        check_lse(lse[b, h], lse_ref, what)
