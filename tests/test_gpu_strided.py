@@ -22,8 +22,11 @@ def _contig(*ts):
     return [t.contiguous() for t in ts]
 
 
-@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 200, 64, False), (1, 4, 384, 128, True), (2, 2, 129, 128, False)])
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 200, 64, False), (1, 4, 384, 128, True), (2, 2, 129, 128, False),
+                                             (2, 80, 700, 64, False), (3, 60, 1000, 128, True)])
 def test_bnhd_matches_contiguous_bitwise(B, H, N, d, causal):
+    """(The last two shapes have more 256-row tiles than SMs: their forward
+    runs the persistent grid, with the same strides.)"""
     q, k, v, do = draw_shape(B, H, N, d, 7 + N, 1.0, "cuda", torch.bfloat16)
     # the same values stored as [B, N, H, d]; the views are [B, H, N, d]
     qs, ks, vs, dos = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (q, k, v, do))
