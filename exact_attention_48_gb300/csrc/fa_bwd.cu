@@ -584,17 +584,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
   uint64_t *do_ready = bars;          // Q and dO written to TMEM by the rows
-  uint64_t *k_full = do_ready + 1;    // [SK]
-  uint64_t *k_empty = k_full + SK;    // [SK]
-  uint64_t *v_full = k_empty + SK;    // [SV]
-  uint64_t *v_empty = v_full + SV;    // [SV]
+  // kv_full[g % SK]: K and V of key block g have both landed (V in its own
+  // ring, stage g % SV): one wait for the MMA thread per block
+  uint64_t *kv_full = do_ready + 1;   // [SK]
+  uint64_t *k_empty = kv_full + SK;   // [SK]
+  uint64_t *v_empty = k_empty + SK;   // [SV]
   uint64_t *s_full = v_empty + SV;
   uint64_t *dp_full = s_full + 1;
   uint64_t *s_free = dp_full + 1;
   uint64_t *ds_ready = s_free + 1;
   uint64_t *dq_done = ds_ready + 1;
   uint64_t *drain = dq_done + 1;
-  static_assert(2 + 2 * SK + 2 * SV + 6 <= L::kNumBars, "barrier slots");
+  static_assert(1 + 2 * SK + SV + 6 <= L::kNumBars, "barrier slots");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
   const WaitCtl ctl{abort_flag, p.status};
@@ -640,11 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(do_ready, kRowWarps);
     for (int s = 0; s < SK; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&kv_full[s], 2);  // the K and the V producer lane
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < SV; ++s) {
-      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
@@ -680,14 +680,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < item_nkv(it); ++j) {
           const int g = issued, st = g % SK;
           if (!(pok = mbar_wait(&k_empty[st], ((g / SK) & 1) ^ 1, ctl, kSiteKEmpty))) break;
-          mbar_arrive_expect_tx(&k_full[st], L::kTile);
+          mbar_arrive_expect_tx(&kv_full[st], L::kTile);
 #pragma unroll
           for (int s = 0; s < L::kSlabs; ++s)
-            tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &k_full[st], s * 64, row0 + j * kBlk, tma_h,
+            tma_load_4d(sK + st * L::kTile + s * kBlk * 128, &tm_k, &kv_full[st], s * 64, row0 + j * kBlk, tma_h,
                         tma_b);
           issued = g + 1;
         }
-      for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&k_full[j % SK], (j / SK) & 1);
+      for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j) mbar_drain(&kv_full[j % SK], (j / SK) & 1);
     } else if (lane == 1) {
       // the V ring
       tma_prefetch_desc(&tm_v);
@@ -697,14 +697,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < item_nkv(it); ++j) {
           const int g = issued, st = g % SV;
           if (!(pok = mbar_wait(&v_empty[st], ((g / SV) & 1) ^ 1, ctl, kSiteVEmpty))) break;
-          mbar_arrive_expect_tx(&v_full[st], L::kTile);
+          mbar_arrive_expect_tx(&kv_full[g % SK], L::kTile);
 #pragma unroll
           for (int s = 0; s < L::kSlabs; ++s)
-            tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &v_full[st], s * 64, row0 + j * kBlk, tma_h,
+            tma_load_4d(sV + st * L::kTile + s * kBlk * 128, &tm_v, &kv_full[g % SK], s * 64, row0 + j * kBlk, tma_h,
                         tma_b);
           issued = g + 1;
         }
-      for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&v_full[j % SV], (j / SV) & 1);
+      for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j) mbar_drain(&kv_full[j % SK], (j / SK) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -740,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_kv = item_nkv(it);
         // the item's Q and dO in TMEM (written by the rows once the previous
         // item's products were complete and its dQ was read out)
-        ok = mbar_wait(&k_full[g0 % SK], (g0 / SK) & 1, ctl, kSiteKFull) &&
-             mbar_wait(&v_full[g0 % SV], (g0 / SV) & 1, ctl, kSiteVFull) && mbar_wait(do_ready, it & 1, ctl, kSiteDoFull);
+        ok = mbar_wait(&kv_full[g0 % SK], (g0 / SK) & 1, ctl, kSiteKvFull) &&
+             mbar_wait(do_ready, it & 1, ctl, kSiteDoFull);
         if (!ok) break;
         tc_fence_after();
         issue_s(g0);
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = j + 1 < n_kv;
           if (more) {
             // S(j+1) once the rows have read S(j)
-            if (!(ok = mbar_wait(&k_full[(g + 1) % SK], ((g + 1) / SK) & 1, ctl, kSiteKFull))) break;
+            if (!(ok = mbar_wait(&kv_full[(g + 1) % SK], ((g + 1) / SK) & 1, ctl, kSiteKvFull))) break;
             if (!(ok = mbar_wait(s_free, g & 1, ctl, kSiteSFull))) break;
             tc_fence_after();
             issue_s(g + 1);
@@ -765,7 +765,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dQ += dS K_j (dS from TMEM over the dP columns; K_j MN-major over
           // d) once the rows have written dS(j), then dP(j+1) over it
           if (!(ok = mbar_wait(ds_ready, g & 1, ctl, kSiteDsReady))) break;
-          if (more && !(ok = mbar_wait(&v_full[(g + 1) % SV], ((g + 1) / SV) & 1, ctl, kSiteVFull))) break;
           tc_fence_after();
           {
             const uint64_t bk = k_mn(g);
