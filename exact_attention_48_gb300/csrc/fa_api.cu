@@ -181,6 +181,11 @@ constexpr long long kMaxGridX = 2147483647LL;  // largest x extent of a launch g
 // B4 H32 N4096 backward 1.690 -> 1.657 ms, while B4 H16 N4096 (heaviest
 // first over all heads) ran 0.7 % slower with them.
 constexpr int kPairMaxBlocksKv = 32, kPairMaxBlocksQ = 16;
+// Non-causal backward: pairs of mirror blocks per CTA up to this many blocks
+// (all CTAs have equal work either way; a pair pays one CTA's fixed cost for
+// two blocks).  Measured, B*N = 16384, H = 16: d = 128 +4 % at N = 512, +3 %
+// at 1024, 0 at 2048, -2 % at 4096; d = 64 +10 %, +5 %, +1 %, -1 %.
+constexpr int kPairMaxBlocksNonCausal = 16;
 // Longest sequence, in 256-row tiles, for which the batched forward runs
 // persistent CTAs.  Measured against one CTA per tile (forward only, L2
 // flushed, B*N = 16384, H = 16):
@@ -408,8 +413,12 @@ fa_status_t bwd_impl(const void *q, const Strides &sq, const void *k, const Stri
   // strict heaviest-first order (measured: B8 H16 N4096 +5..9 %, B1 H16
   // N16384 -2 %).
   p.head_major = (static_cast<long long>(BH) * (p.num_blk + 1) > 3040) ? 1 : 0;
-  p.pairs_kv = (causal && p.num_blk <= kPairMaxBlocksKv) ? 1 : 0;
-  p.pairs_q = (causal && (p.num_blk <= kPairMaxBlocksQ || (p.head_major && p.num_blk <= kPairMaxBlocksKv))) ? 1 : 0;
+  if (causal) {
+    p.pairs_kv = (p.num_blk <= kPairMaxBlocksKv) ? 1 : 0;
+    p.pairs_q = (p.num_blk <= kPairMaxBlocksQ || (p.head_major && p.num_blk <= kPairMaxBlocksKv)) ? 1 : 0;
+  } else {
+    p.pairs_kv = p.pairs_q = (p.num_blk <= kPairMaxBlocksNonCausal) ? 1 : 0;
+  }
   fa_status_t rc = FA_OK;
   const cudaEvent_t ev[3] = {t_bwd_ev[0], t_bwd_ev[1], t_bwd_ev[2]};
   t_bwd_ev[0] = t_bwd_ev[1] = t_bwd_ev[2] = nullptr;

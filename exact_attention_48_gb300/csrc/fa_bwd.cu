@@ -21,7 +21,7 @@
 //                          the key blocks (3 products per block).
 // The dQ kernel reads only the inputs and the pre-kernel's statistics, so
 // it runs on a side stream next to the dK/dV kernel (forked from and joined
-// back to the caller's stream).  On short causal sequences both kernels
+// back to the caller's stream).  On short sequences both kernels
 // give each CTA a pair of mirror blocks of one head instead of one block.
 // Splitting dQ off costs two recomputed products per block pair but removes
 // the fp32 reduction of dQ across key blocks through L2, which otherwise
@@ -200,17 +200,16 @@ __global__ void __launch_bounds__(KvRows<RG>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
-  // Tile order.  Causal with pairs (short sequences): a CTA takes two key
-  // blocks of one head, j and its mirror nb-1-j (one block when they
-  // coincide), which see nb + 1 query blocks together whatever j is: every
-  // CTA has the same work, and the second block's start overlaps the first
-  // one's end; the CTAs of a head run together.  Causal otherwise: one key
-  // block per CTA, the blocks with the most query blocks (j small) first,
-  // across all heads -- or head by head when the heaviest block is short
-  // against each SM's share of the work, so that the blocks running
-  // together share their Q and dO in L2.  Non-causal: the key blocks of one
-  // head run together.
-  static_assert(CAUSAL || !PAIRS, "pairs are a causal schedule");
+  // Tile order.  With pairs (short sequences): a CTA takes two key blocks of
+  // one head, j and its mirror nb-1-j (one block when they coincide); causal,
+  // they see nb + 1 query blocks together whatever j is, so every CTA has
+  // the same work; the second block's start overlaps the first one's end,
+  // and the CTAs of a head run together.  Causal otherwise: one key block
+  // per CTA, the blocks with the most query blocks (j small) first, across
+  // all heads -- or head by head when the heaviest block is short against
+  // each SM's share of the work, so that the blocks running together share
+  // their Q and dO in L2.  Non-causal: the key blocks of one head run
+  // together.
   constexpr bool pairs = PAIRS;
   int bh, j0;
   if (pairs) {
@@ -604,13 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nblk = p.num_blk;  // blocks of the longest sequence (the padding of the row statistics)
 
-  // Tile order.  Causal with pairs (short sequences): a CTA takes the
-  // query blocks nb-1-i and i of one head (one block when they coincide),
-  // which see nb + 1 key blocks together; the CTAs of a head run together.
-  // Causal otherwise: the query blocks with the most key blocks (i large)
-  // first, across all heads or head by head (as the dK/dV kernel).
-  // Non-causal: the query blocks of one head run together.
-  static_assert(CAUSAL || !PAIRS, "pairs are a causal schedule");
+  // Tile order.  With pairs (short sequences): a CTA takes the query blocks
+  // nb-1-i and i of one head (one block when they coincide; causal, they see
+  // nb + 1 key blocks together); the CTAs of a head run together.  Causal
+  // otherwise: the query blocks with the most key blocks (i large) first,
+  // across all heads or head by head (as the dK/dV kernel).  Non-causal: the
+  // query blocks of one head run together.
   constexpr bool pairs = PAIRS;
   int bh, i0;  // i0: the first item's query block (pairs: its mirror's index)
   if (pairs) {
@@ -985,19 +983,18 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
       <<<static_cast<unsigned>(pre_blocks < kPreGridMax ? pre_blocks : kPreGridMax), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // one CTA per block, or (causal with pairs) per pair of mirror blocks
+  // one CTA per block, or (pairs) per pair of mirror blocks
   const unsigned grid_kv = static_cast<unsigned>(p.BH) *
-                           static_cast<unsigned>((CAUSAL && p.pairs_kv) ? (p.num_blk + 1) / 2 : p.num_blk);
+                           static_cast<unsigned>(p.pairs_kv ? (p.num_blk + 1) / 2 : p.num_blk);
   const unsigned grid_q = static_cast<unsigned>(p.BH) *
-                          static_cast<unsigned>((CAUSAL && p.pairs_q) ? (p.num_blk + 1) / 2 : p.num_blk);
+                          static_cast<unsigned>(p.pairs_q ? (p.num_blk + 1) / 2 : p.num_blk);
   // (long non-causal heads: four row groups; causal: two, see KvRows)
   constexpr int RG = CAUSAL ? 2 : 4;
   // the schedule is a template parameter: the one-block kernels carry no
   // loop over items (measured 3-4 % faster than a run-time flag)
-  const auto kern_kv = (CAUSAL && p.pairs_kv) ? fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, CAUSAL>
-                                              : fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, false>;
-  const auto kern_q = (CAUSAL && p.pairs_q) ? fa_bwd_dq_kernel<D, CAUSAL, VARLEN, CAUSAL>
-                                            : fa_bwd_dq_kernel<D, CAUSAL, VARLEN, false>;
+  const auto kern_kv = p.pairs_kv ? fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, true>
+                                  : fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN, RG, false>;
+  const auto kern_q = p.pairs_q ? fa_bwd_dq_kernel<D, CAUSAL, VARLEN, true> : fa_bwd_dq_kernel<D, CAUSAL, VARLEN, false>;
   if (concurrent && !ev) {
     // The dQ kernel reads only the inputs and the pre-kernel's statistics,
     // so it runs on a side stream next to the dK/dV kernel: each grid is

@@ -74,24 +74,26 @@ def test_varlen_against_oracle():
                 check_grad(g[s:e, h], r, name, what)
 
 
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("d", [64, 128])
-def test_causal_backward_same_bits_with_and_without_block_pairs(d):
-    """The causal backward of short sequences runs two mirror blocks (j and
-    nb-1-j) per CTA -- up to 32 blocks per sequence in the dK/dV kernel and
-    16 in the dQ kernel -- and of longer ones one block per CTA.  In a pack
-    whose longest sequence is past both limits every sequence runs one block
-    per CTA, while each short sequence alone runs in pairs: the tiles'
-    arithmetic is the same either way, so the bits must be."""
+def test_backward_same_bits_with_and_without_block_pairs(d, causal):
+    """The backward of short sequences runs two mirror blocks (j and nb-1-j)
+    per CTA -- causal: up to 32 blocks per sequence in the dK/dV kernel and
+    16 in the dQ kernel; non-causal: up to 16 in both -- and of longer ones
+    one block per CTA.  In a pack whose longest sequence is past those limits
+    every sequence runs one block per CTA, while each short sequence alone
+    runs in pairs: the tiles' arithmetic is the same either way, so the bits
+    must be."""
     lengths = [4200, 1000, 2100, 300, 129, 1]  # blocks: 33, 8, 17, 3, 2, 1
     H = 2
     q, k, v, do, cu = _pack(lengths, H, d, 41 + d)
-    o, lse = fa_fwd_varlen(q, k, v, cu, max(lengths), True)
-    dq, dk, dv = fa_bwd_varlen(q, k, v, o, do, lse, cu, max(lengths), True)
+    o, lse = fa_fwd_varlen(q, k, v, cu, max(lengths), causal)
+    dq, dk, dv = fa_bwd_varlen(q, k, v, o, do, lse, cu, max(lengths), causal)
     assert fa_device_status() == 0
     for b in range(1, len(lengths)):
         qs, ks, vs, dos = (_seq(t, cu, b) for t in (q, k, v, do))
-        o_r, lse_r = fa_fwd(qs, ks, vs, True)
-        g_r = fa_bwd(qs, ks, vs, o_r, dos, lse_r, True)
+        o_r, lse_r = fa_fwd(qs, ks, vs, causal)
+        g_r = fa_bwd(qs, ks, vs, o_r, dos, lse_r, causal)
         assert torch.equal(_seq(o, cu, b), o_r), f"o of sequence {b}"
         for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), g_r):
             assert torch.equal(_seq(g, cu, b), r), f"{name} of sequence {b} ({lengths[b]} rows)"
