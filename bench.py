@@ -210,8 +210,11 @@ def oracle_fp8_sample(w, rows, nthreads=None):
 def cpu_baseline(w, target_s=12.0):
     if w.layout == "fp8":
         dt, fl, nt = oracle_fp8_sample(w, 64)
-        rows = int(min(w.N, max(64, target_s * fl / max(dt, 1e-6) / (4.0 * w.N * w.d))))
-        dt, fl, nt = oracle_fp8_sample(w, rows)
+        for _ in range(2):  # (two passes, as below)
+            rows = int(min(w.N, max(64, target_s * fl / max(dt, 1e-6) / (4.0 * w.N * w.d))))
+            dt, fl, nt = oracle_fp8_sample(w, rows)
+            if dt >= 0.5 * target_s or rows >= w.N:
+                break
         return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
                 "sample": f"FP8 forward of query rows 0..{rows - 1} of head (0,0) against all {w.N} keys, "
                           f"d={w.d}, fp64 C oracle (e4m3 definition), {dt:.1f} s"}
@@ -221,12 +224,18 @@ def cpu_baseline(w, target_s=12.0):
         return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
                 "sample": f"forward of {heads} of the {w.B * w.H} heads ({w.nq} query row(s) against all {w.N} "
                           f"cached keys, d={w.d}), repeated {calls} times, fp64 C oracle, {dt:.1f} s"}
-    # calibrate on a small sample, then size the timed one to ~target_s
+    # calibrate on a small sample, then size the timed one to ~target_s (a
+    # second pass: the small sample's rate understates the threads' rate on
+    # a larger one)
     dt, fl, nt = oracle_sample(w, 64)
-    rate = fl / max(dt, 1e-6)
-    rows = int(min(w.N, max(64, target_s * rate / (4.0 * w.N * w.d * 3.5))))
-    rows = max(64, rows // 64 * 64)
-    dt, fl, nt = oracle_sample(w, rows)
+    rows = 64
+    for _ in range(2):
+        rate = fl / max(dt, 1e-6)
+        rows = int(min(w.N, max(64, target_s * rate / (4.0 * w.N * w.d * 3.5))))
+        rows = max(64, rows // 64 * 64)
+        dt, fl, nt = oracle_sample(w, rows)
+        if dt >= 0.5 * target_s or rows >= w.N:
+            break
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
             "sample": f"fwd+bwd of query rows 0..{rows - 1} of head (0,0) against all {w.N} keys, "
                       f"d={w.d}, non-causal, fp64 C oracle, {dt:.1f} s"}
