@@ -79,17 +79,20 @@ def test_fwd_deterministic():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_fwd_guard_bands():
-    """Writes stay inside o and lse: canaries around both survive."""
-    B, H, N, d = 1, 3, 300, 64
+@pytest.mark.parametrize("H,d,causal", [(3, 64, False), (160, 64, False), (160, 128, True)])
+def test_fwd_guard_bands(H, d, causal):
+    """Writes stay inside o and lse: canaries around both survive (160 heads:
+    the persistent grid, whose CTAs write several tiles' rows)."""
+    B, N = 1, 300
     q, k, v, _ = draw_shape(B, H, N, d, 5, 1.0, "cuda", torch.bfloat16, with_dout=False)
     pad = 4096
     ob = torch.full((B * H * N * d + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
     lb = torch.full((B * H * N + 2 * pad,), 7.0, device="cuda")
     o = ob[pad:pad + B * H * N * d].view(B, H, N, d)
     lse = lb[pad:pad + B * H * N].view(B, H, N)
-    fa_fwd(q, k, v, False, o=o, lse=lse)
+    fa_fwd(q, k, v, causal, o=o, lse=lse)
     torch.cuda.synchronize()
+    assert fa_device_status() == 0
     assert torch.all(ob[:pad] == 7) and torch.all(ob[-pad:] == 7)
     assert torch.all(lb[:pad] == 7) and torch.all(lb[-pad:] == 7)
 
@@ -137,3 +140,25 @@ def test_fwd_persistent_same_bits_as_one_cta_per_tile(B, H, N, d, causal):
         what = f"persistent B={B} H={H} N={N} d={d} causal={causal} head ({b}, {h})"
         check_o(o[b, h], o_ref, what)
         check_lse(lse[b, h], lse_ref, what)
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_fwd_persistent_scale_values(scale):
+    """The persistent grid with a negative and a zero scale (the running
+    minimum path and uniform weights), causal and not: the same bits as the
+    packed call's one CTA per tile, and two heads against the oracle."""
+    B, H, N, d = 1, 160, 300, 64
+    q, k, v, _ = draw_shape(B, H, N, d, 77, 1.0, "cuda", torch.bfloat16, with_dout=False)
+    qp, kp, vp = (t.transpose(1, 2).reshape(B * N, H, d).contiguous() for t in (q, k, v))
+    cu = torch.tensor([0, N], dtype=torch.int32, device="cuda")
+    for causal in (False, True):
+        o, lse = fa_fwd(q, k, v, causal, scale)
+        o_p, lse_p = fa_fwd_varlen(qp, kp, vp, cu, N, causal, scale)
+        assert fa_device_status() == 0
+        assert torch.equal(o_p.reshape(B, N, H, d).transpose(1, 2), o)
+        assert torch.equal(lse_p.reshape(H, B, N).permute(1, 0, 2), lse)
+        for h in (0, H - 1):
+            o_ref, lse_ref = oracle.fwd(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), causal, scale)
+            spread = oracle.fwd_spread(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), causal, scale)
+            check_o(o[0, h], o_ref, f"persistent scale={scale} causal={causal} head {h}", spread)
+            check_lse(lse[0, h], lse_ref, f"persistent scale={scale} causal={causal} head {h}")
