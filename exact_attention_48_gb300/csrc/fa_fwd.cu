@@ -357,8 +357,8 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams &p, int x) {
   return t;
 }
 
-// PERSIST: one CTA per SM walks the tiles (round r = 0, 1, ... takes tile
-// r * gridDim.x + blockIdx.x, mirrored in odd rounds when causal);
+// PERSIST: one CTA per SM walks the tiles (its turn r = 0, 1, ... takes
+// tile r * gridDim.x + blockIdx.x, mirrored in odd turns when causal);
 // otherwise one CTA per tile.  At d = 64 the persistent kernel keeps two Q
 // buffers, so the next tile's Q arrives while the current tile is worked
 // on, and its first scores are formed while the softmax warps still write
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = FwdLayout<D, QB>;
   constexpr int S = L::kStages;
   // tiles a CTA takes at most (the persistent loop ends on the tile count)
-  constexpr int kRounds = PERSIST ? 0x7fffffff : 1;
+  constexpr int kTurns = PERSIST ? 0x7fffffff : 1;
   const int num_tiles = p.BH * p.num_qblk;
 
   extern __shared__ uint8_t smem_raw[];
@@ -407,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     own = fwd_tile<CAUSAL, VARLEN>(p, static_cast<int>(blockIdx.x));
     if (own.empty) return;
   }
-  // Persistent CTAs take tile r * G + c in round r (G CTAs, c = blockIdx);
-  // causal tiles come heaviest first, and odd rounds run c backwards so that
+  // Persistent CTAs take tile r * G + c in turn r (G CTAs, c = blockIdx);
+  // causal tiles come heaviest first, and odd turns run c backwards so that
   // each CTA's heavy and light tiles even out.
   auto tile_index = [&](int r) -> int {
     const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // K/V blocks loaded so far, over all tiles (ring position)
       int q_issued = 0, k_issued = 0, v_issued = 0;
       bool run = true;
-      for (int r = 0; run && r < kRounds; ++r) {
+      for (int r = 0; run && r < kTurns; ++r) {
         const int x = tile_index(r);
         if (PERSIST && x >= num_tiles) break;
         const FwdTile tl = tile_at(x);
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;           // ring position of the current tile's first K/V block
       int c0 = 0, c1 = 0;  // blocks tiles 0 and 1 finished in earlier tiles (barrier phases)
       bool ok = true;
-      for (int r = 0; ok && r < kRounds; ++r) {
+      for (int r = 0; ok && r < kTurns; ++r) {
         const int x = tile_index(r);
         if (PERSIST && x >= num_tiles) break;
         const FwdTile tl = tile_at(x);
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
     int cb = 0;  // blocks this tile's barriers completed in earlier tiles
-    for (int r = 0; r < kRounds; ++r) {
+    for (int r = 0; r < kTurns; ++r) {
       const int x = tile_index(r);
       if (PERSIST && x >= num_tiles) break;
       const FwdTile tl = tile_at(x);

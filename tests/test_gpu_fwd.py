@@ -122,7 +122,7 @@ def test_fwd_persistent_same_bits_as_one_cta_per_tile(B, H, N, d, causal):
     arithmetic is the same either way, so the bits must be.  The shapes give
     ragged last tiles, single-key heads and tile counts that are not
     multiples of the SM count (some CTAs take one tile more than others);
-    heads of the first and the last round are also checked against the
+    heads of the first and the last turn are also checked against the
     oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert B * H * ((N + 255) // 256) > sms
